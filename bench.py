@@ -1,0 +1,434 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused ZeRO reduce-scatter + Adam + all-gather step.
+
+One step = one call of ``zero_adam_step`` (all P simulated ranks' shards:
+reduce-scatter of the fp16 gradients, fp32 Adam, fp16 cast, write into the
+gathered parameter vector) over one batch of synthetic gradients.  The
+default workload is the GPT-2-small sized flat vector: N = 124,439,808
+parameters, P = 8 ranks, ZeRO-1, standard Adam, gradients ~ N(0, 1e-3) with
+1 % of entries x100.
+
+Printed: one JSON line (rank 0).  ``value`` is parameters updated per second
+over the whole job with every input resident in HBM; ``e2e`` is the same
+metric with each step's gradients copied from pinned host memory and the
+gathered fp16 parameters copied back inside the timed region;
+``roofline`` rates the fused kernel against the measured HBM copy bandwidth;
+``cpu_baseline`` times the CPU oracle on a bounded sample on the host cores.
+
+``--impl reference`` times the CPU oracle instead (the only other
+implementation of this step), on the same workload and metric.
+
+Multi-GPU (torchrun): every rank runs its own independent replica of the
+whole simulated step on its own GPU -- the path has no exchange between
+GPUs -- and ``value`` counts all ranks' parameters over the slowest rank's
+time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+NOMINAL_HBM_GBS = 8000.0
+DEFAULT_STEPS = {"tiny": 20000, "gpt2s": 2500, "tf1p3b": 200, "shard7p5b": 800, "folded": 600}
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SRC = os.path.join(ROOT, "zero_sharded_mixed_shard_gb300", "csrc", "step.cu")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="gpt2s",
+                    choices=("tiny", "gpt2s", "tf1p3b", "shard7p5b", "folded"))
+    ap.add_argument("--mode", type=int, default=None, help="Adam reading (default: the workload's first)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="wall time budget of the CPU-oracle leg")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.workload]
+    return args
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU under torchrun)
+# ---------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float, device=None) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.proc = None
+        self.out = None
+        self.gpu = gpu_index
+        self.period = period_ms
+
+    def start(self):
+        import tempfile
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = []
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except (ValueError, IndexError):
+                continue
+        os.unlink(self.out.name)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in inside for i, s in enumerate(r[3]) if s == "Active"})
+        return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
+                "sm_max_mhz": max((r[2] for r in inside), default=None),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# roofline helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel source."""
+    path = os.path.join(PROFILE_DIR, f"zero_fused_step_{workload}.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha256") != kernel_source_hash():
+            return None
+        return float(kv["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle leg (used by cpu_baseline and by --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_rate(wl, mode: int, budget_s: float, sample: int | None = None, steps: int | None = None):
+    """Time the oracle (as it stands, all host cores) on the first ``sample``
+    elements of the workload, all P ranks.  Returns (params/s, cores, sample,
+    per-step seconds list)."""
+    import numpy as np
+
+    import oracle
+    from zero_sharded_mixed_shard_gb300 import synth
+    oracle.build()
+    cores = os.cpu_count() or 1
+    if sample is None:
+        sample = min(wl.elems, 1 << 24)
+    codes = synth.np_grads(wl.P, sample, sample, wl.grad_sigma, wl.seed,
+                           wl.heavy_tail_frac, wl.zero_frac)
+    w, m, v, _ = synth.np_state(sample, wl.seed, wl.master_sigma)
+    out = np.empty(sample, np.uint16)
+    times = []
+    t = 0
+    start = time.perf_counter()
+    while True:
+        t += 1
+        t0 = time.perf_counter()
+        oracle.adam_elems(codes, sample, wl.P, w, m, v, t, wl.lr, wl.b1, wl.b2, wl.eps, mode,
+                          threads=cores, params_out=out)
+        times.append(time.perf_counter() - t0)
+        if steps is not None:
+            if t >= steps:
+                break
+        elif time.perf_counter() - start >= budget_s:
+            break
+    return sample * len(times) / sum(times), cores, sample, times
+
+
+def run_reference(args, wl, mode, dist):
+    """--impl reference: the CPU oracle on the same workload, rank 0 only."""
+    if dist.rank != 0:
+        return 0
+    # size each step's sample so the whole run stays within ~90 s of host time
+    rate, cores, _, _ = oracle_rate(wl, mode, 0.0, sample=min(wl.elems, 1 << 22), steps=1)
+    per_step = 90.0 / (args.steps + args.warmup)
+    sample = int(min(wl.elems, 1 << 24, max(4096, rate * per_step)))
+    _, cores, sample, times = oracle_rate(wl, mode, 0.0, sample=sample,
+                                          steps=args.steps + args.warmup)
+    timed = times[args.warmup:]
+    sec = sum(timed)
+    value = sample * len(timed) / sec
+    line = {
+        "impl": "reference",
+        "metric": "params updated/sec and achieved HBM GB/s (% of GB300 peak) per Adam step",
+        "value": value, "unit": "params/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(timed), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(wl, mode, sample_note=f"first {sample} elements per step"),
+        "achieved_gbs": value * wl.bytes_per_elem / 1e9,
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": cores, "kind": "oracle",
+                         "sample": f"elements [0, {sample}) of the {wl.name} workload, all "
+                                   f"{wl.P} ranks, one oracle call per step"},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl, mode, sample_note=None):
+    cfg = {"workload": f"{wl.name}: N={wl.N:,} P={wl.P} ZeRO-{wl.stage} "
+                       f"{'shard ' + str(wl.shard) + ' only, ' if wl.shard is not None else ''}"
+                       f"Adam mode {mode}",
+           "N": wl.N, "elements_per_step": wl.elems, "P": wl.P, "stage": wl.stage, "mode": mode,
+           "rank_stride": wl.rank_stride(True), "bytes_per_elem": wl.bytes_per_elem,
+           "l2": f"inputs larger than L2: {wl.elems * wl.bytes_per_elem / 1e9:.2f} GB moved per step"}
+    if sample_note:
+        cfg["sample"] = sample_note
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, wl, mode, dist):
+    import torch
+
+    import zero_sharded_mixed_shard_gb300 as z
+    from zero_sharded_mixed_shard_gb300 import synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the fused step has no CPU path)")
+    torch.cuda.set_device(dist.local_rank)
+    dist.init("nccl")
+    device = torch.device("cuda", dist.local_rank)
+    z.lib()
+
+    E, P = wl.elems, wl.P
+    stride = wl.rank_stride(True)
+    g = synth.torch_grads(P, E, stride, wl.grad_sigma, wl.seed + 17 * dist.rank, device,
+                          wl.heavy_tail_frac, wl.zero_frac, step=1)
+    master, m, v, params = synth.torch_state(E, wl.seed + 17 * dist.rank, device, wl.master_sigma)
+    stream = torch.cuda.current_stream(device)
+
+    def step(t):
+        if wl.shard is None:
+            z.zero_adam_step(g, stride, master, m, v, params, wl.N, P, wl.stage, t, wl.lr,
+                             wl.b1, wl.b2, wl.eps, mode, stream)
+        else:
+            z.zero_adam_step_shard(g, stride, 0, wl.shard, master, m, v, params, wl.N, P,
+                                   wl.stage, t, wl.lr, wl.b1, wl.b2, wl.eps, mode, stream)
+
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        step(t)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(dist.local_rank)
+    if dist.rank == 0:
+        sampler.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    h0 = time.time()
+    for i in range(K):
+        t += 1
+        starts[i].record(stream)
+        step(t)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    h1 = time.time()
+    dist.barrier()
+    clocks = sampler.stop(h0, h1) if dist.rank == 0 else None
+    region_ms = starts[0].elapsed_time(ends[-1])
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    region_ms = dist.max(region_ms, device)
+    mean_launch_ms = dist.max(sum(launch_ms) / K, device)
+
+    elems_total = E * K * dist.world
+    value = elems_total / (region_ms / 1e3)
+    alg_bytes = E * wl.bytes_per_elem
+    achieved = alg_bytes / (mean_launch_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(z, wl, mode, g, master, m, v, params, stride, stream, device, dist, t,
+                      K_e2e=max(3, min(K, 100)))
+
+    del g
+    torch.cuda.empty_cache()
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        rate, cores, sample, times = oracle_rate(wl, mode, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "params/s", "cores": cores, "kind": "oracle",
+               "sample": f"elements [0, {sample}) of the {wl.name} workload, all {P} ranks, "
+                         f"{len(times)} consecutive steps in {sum(times):.1f} s"}
+
+    if dist.rank == 0:
+        traffic = profiled_traffic(wl.name)
+        line = {
+            "metric": "params updated/sec and achieved HBM GB/s (% of GB300 peak) per Adam step",
+            "value": value, "unit": "params/s", "n_gpus": dist.world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": region_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "io_dtypes": "fp16 gradients and parameters, fp32 master/m/v",
+            "data": "synthetic (seeded device RNG)",
+            "config": workload_config(wl, mode),
+            "achieved_hbm_gbs": alg_bytes * K * dist.world / (region_ms / 1e3) / 1e9,
+            "pct_of_nominal_8tbs": 100 * alg_bytes * K / (region_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "zero_fused_step_kernel",
+                         "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                         "algorithmic_bytes_per_launch": alg_bytes,
+                         "mean_launch_ms": mean_launch_ms},
+            "gpu_launches": K,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+def run_e2e(z, wl, mode, g, master, m, v, params, stride, stream, device, dist, t, K_e2e):
+    """Each step: pinned host gradients -> device, the step, gathered fp16
+    parameters -> pinned host; all inside the timed region."""
+    import torch
+    host_g = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+    host_g.copy_(g)
+    host_p = torch.empty(params.shape, dtype=params.dtype, pin_memory=True)
+    dev_g = g
+    for _ in range(2):   # warm the copy engines
+        dev_g.copy_(host_g, non_blocking=True)
+        host_p.copy_(params, non_blocking=True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K_e2e):
+        t += 1
+        dev_g.copy_(host_g, non_blocking=True)
+        if wl.shard is None:
+            z.zero_adam_step(dev_g, stride, master, m, v, params, wl.N, wl.P, wl.stage, t, wl.lr,
+                             wl.b1, wl.b2, wl.eps, mode, stream)
+        else:
+            z.zero_adam_step_shard(dev_g, stride, 0, wl.shard, master, m, v, params, wl.N, wl.P,
+                                   wl.stage, t, wl.lr, wl.b1, wl.b2, wl.eps, mode, stream)
+        host_p.copy_(params, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(e0.elapsed_time(e1), device)
+    return {"value": wl.elems * K_e2e * dist.world / (ms / 1e3), "unit": "params/s",
+            "h2d_bytes_per_step": host_g.numel() * host_g.element_size(),
+            "d2h_bytes_per_step": host_p.numel() * host_p.element_size(),
+            "steps": K_e2e, "ms_per_step": ms / K_e2e}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from zero_sharded_mixed_shard_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    mode = wl.modes[0] if args.mode is None else args.mode
+    dist = Dist()
+    if args.impl == "reference":
+        return run_reference(args, wl, mode, dist)
+    return run_ours(args, wl, mode, dist)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

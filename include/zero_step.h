@@ -1,0 +1,209 @@
+/*
+ * zero_step.h -- C ABI of the fused ZeRO partitioned mixed-precision Adam step
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * P data-parallel ranks are simulated on one GPU: each holds an fp16 local
+ * gradient in device memory.  For every shard k of the flat parameter vector
+ * (M = ceil(N/P) elements, the last one shorter or empty) one pass
+ *   1. reduce-scatters: averages the P gradient slices of the shard in fp32,
+ *      rank order 0..P-1;
+ *   2. runs Adam on the fp32 master / momentum / variance shard;
+ *   3. casts the new weights to fp16 (round to nearest, ties to even);
+ *   4. writes them into the fp16 parameter vector at the shard's offset,
+ *      which is the all-gather's output.
+ * No intermediate gradient buffer is written: the mean lives in registers.
+ *
+ * Sources (page title, section):
+ *  [P1] 深度学习专题：模型训练的数据并行（三） §（一）Adam 优化器 (update and
+ *       moment equations, beta defaults, m0 = v0 = 0); §（二） (storage per
+ *       GPU for plain data parallel); §（三）-（五） ZeRO-1/2/3 优化原理
+ *       (ceil partition M = ceil(N/P), s_k = 1+(k-1)M .. e_k = kM, the
+ *       reduce-scatter / update / all-gather steps, float counts per GPU).
+ *  [P2] ZeRO 原理：把模型状态切到多张 GPU 上 (7.5B parameters on 64 GPUs:
+ *       120 / 31.4 / 16.6 / 1.9 GB; fp32 master cast back to fp16 on the
+ *       owning GPU).
+ *  [P3] ZeRO 技术原理：进阶与 Offload §1.1.5 Reduce-Scatter, §1.1.6
+ *       All-Gather, §1.4 显存分析 (16Φ bytes; P_os, P_os+g, P_os+g+p),
+ *       §1.5 通信数据量分析 (2Φ / 3Φ per card), reference [10] Kingma & Ba.
+ *  [P4] 高效AI 第19讲：分布式训练（第一部分） 通信原语 All-Reduce
+ *       (g = (1/N) Σ g_i), ZeRO 和 FSDP (bytes per parameter).
+ *
+ * General rules for every function below:
+ *  - Return 0 (ZERO_OK) on success or a negative ZERO_E* code; the code's
+ *    text is zero_strerror(code).  A rejected call has no side effects.
+ *  - Device pointers are caller-owned (for example torch tensors).  The
+ *    library never allocates, frees or synchronises device memory; kernels
+ *    are enqueued on the caller's stream and the call returns immediately.
+ *  - Element counts and strides are in elements, not bytes.
+ *  - fp16 buffers are passed as void* holding IEEE binary16 codes.
+ */
+#ifndef ZERO_STEP_H
+#define ZERO_STEP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Status codes                                                             */
+/* ------------------------------------------------------------------------ */
+#define ZERO_OK 0
+#define ZERO_EINVAL (-1)   /* bad argument: null pointer, size, stage, mode, t, hyper-parameter */
+#define ZERO_EALIGN (-2)   /* a pointer is not aligned to its element size (4 B fp32, 2 B fp16) */
+#define ZERO_EOVERLAP (-3) /* output buffers overlap each other or the gradients */
+#define ZERO_ECUDA (-4)    /* the CUDA runtime rejected the launch (see zero_last_cuda_error) */
+#define ZERO_ENOMEM (-5)   /* host allocation for a layout table failed */
+
+#define ZERO_MAX_RANKS 1024 /* largest P accepted */
+
+/* Adam readings (see zero_adam_step). */
+#define ZERO_MODE_STANDARD 0       /* m, v are raw moving averages; bias-corrected in the update */
+#define ZERO_MODE_FOLDED_LITERAL 1 /* [P1] §（一） as printed: recursion on the divided m, v */
+#define ZERO_MODE_FOLDED_STORAGE 2 /* stored m, v are bias-corrected; recursion on the raw average */
+
+/* ------------------------------------------------------------------------ */
+/* Layout table (host only, no CUDA)                                        */
+/* ------------------------------------------------------------------------ */
+
+/* One piece of a flattened tensor that lies inside one shard. */
+typedef struct {
+    int64_t tensor_id;     /* index into the tensor list given to zero_init_layout */
+    int64_t tensor_offset; /* first element of the piece within the tensor */
+    int64_t shard_offset;  /* first element of the piece within the shard */
+    int64_t len;           /* elements in the piece (> 0) */
+} zero_segment_t;
+
+/* The ceil partition of a flat vector built from a list of tensors, the
+ * pieces of tensors each shard holds, and the per-rank accounting of the
+ * pages.  Filled by zero_init_layout; every array is host memory owned by
+ * the table and released by zero_free_layout. */
+typedef struct {
+    int64_t N;              /* total elements (sum of tensor sizes) */
+    int64_t M;              /* ceil(N / P): the size of every shard but the trailing ones */
+    int32_t P;              /* ranks */
+    int32_t stage;          /* 0 = plain data parallel, 1/2/3 = ZeRO-1/2/3 */
+    int32_t n_tensors;
+    int32_t reserved;
+    int64_t* shard_begin;   /* [P] first element of shard k: min(k*M, N) */
+    int64_t* shard_end;     /* [P] one past the last: min((k+1)*M, N); begin == end when empty */
+    int64_t* seg_offsets;   /* [P+1] shard k's pieces are segs[seg_offsets[k] .. seg_offsets[k+1]) */
+    zero_segment_t* segs;   /* pieces in flat order */
+    int64_t n_segs;
+    double bytes_per_rank_mixed; /* model-state bytes per rank, K = 12 ([P3] §1.4) */
+    double floats_per_rank_p1;   /* float count per rank ([P1] §（二）-（五）) */
+    double comm_elems_per_rank;  /* elements sent + received per rank per step ([P3] §1.5) */
+} zero_layout_t;
+
+/* Build the layout table of the flat vector formed by concatenating
+ * n_tensors tensors of tensor_numel[i] elements (each >= 0, total >= 1),
+ * partitioned over P ranks ([P1] §（三） 准备步骤, 0-based: shard k is
+ * [min(kM,N), min((k+1)M,N)); a shard past the end is empty).
+ * stage selects the accounting only.  On success *out owns heap memory that
+ * must be released with zero_free_layout.  Errors: ZERO_EINVAL (null
+ * pointer, n_tensors < 1, a negative size, N < 1, P outside
+ * [1, ZERO_MAX_RANKS], stage outside [0, 3]); ZERO_ENOMEM. */
+int zero_init_layout(const int64_t* tensor_numel, int32_t n_tensors, int32_t P,
+                     int32_t stage, zero_layout_t* out);
+
+/* Release the arrays of a table filled by zero_init_layout and zero its
+ * fields.  Accepts NULL and an already-freed table. */
+void zero_free_layout(zero_layout_t* layout);
+
+/* Shard bounds without a table: *begin = min(k*M, N), *end = min((k+1)*M, N)
+ * with M = ceil(N/P).  Errors: ZERO_EINVAL (null output, N < 1, P outside
+ * [1, ZERO_MAX_RANKS], k outside [0, P)). */
+int zero_shard_range(int64_t N, int32_t P, int32_t k, int64_t* begin, int64_t* end);
+
+/* Per-rank accounting for N parameters over P ranks at a ZeRO stage:
+ *  *bytes_mixed  fp16 parameters + fp16 gradients + 12 bytes of fp32 Adam
+ *                state per parameter, divided by stage: 16N, 4N + 12N/P,
+ *                2N + 14N/P, 16N/P ([P3] §1.4; [P4] ZeRO 和 FSDP);
+ *  *floats_p1    untyped float count: 4N, 2M + 2N, 3M + N, 4M ([P1]);
+ *  *comm_elems   elements moved per rank per step: 2N for stages 0-2, 3N
+ *                for stage 3 ([P3] §1.5).
+ * Any output pointer may be NULL.  Errors: ZERO_EINVAL (N < 1, P outside
+ * [1, ZERO_MAX_RANKS], stage outside [0, 3]). */
+int zero_memory_bytes(int64_t N, int32_t P, int32_t stage, double* bytes_mixed,
+                      double* floats_p1, double* comm_elems);
+
+/* ------------------------------------------------------------------------ */
+/* The fused step (device)                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* One ZeRO optimizer step over the whole flat vector: all P shards' updates
+ * in one launch on `cuda_stream` (a cudaStream_t; NULL = legacy default).
+ *
+ *  grads_fp16   device, fp16 [P][rank_stride]: rank r's local gradient of the
+ *               N parameters starts at element r * rank_stride (read only).
+ *  rank_stride  elements between ranks, >= N.  A multiple of 8 lets every
+ *               rank's slice share one 16-byte phase (the fast path); any
+ *               value is accepted.
+ *  master, m, v device fp32 [N], read and written in place.
+ *  params_fp16  device fp16 [N], written (never read): element i receives
+ *               fp16(new master[i]) -- shard k's values land at [kM, ...),
+ *               i.e. this buffer is the all-gather's output.
+ *  N            parameters (>= 1);  P  ranks, 1 <= P <= ZERO_MAX_RANKS.
+ *  stage        0..3; documents the buffer roles and does not change any
+ *               result (every stage computes the same bytes).
+ *  t            1-based index of the update being produced (first step: 1).
+ *  lr, beta1, beta2, eps   Adam hyper-parameters; finite, 0 <= beta < 1,
+ *               eps >= 0 ([P1] §（一）: eps is added outside the sqrt).
+ *  mode         ZERO_MODE_STANDARD, ZERO_MODE_FOLDED_LITERAL or
+ *               ZERO_MODE_FOLDED_STORAGE.
+ *
+ * Per element i, every operation a separately rounded fp32 operation
+ * (no contraction), in this order:
+ *   g  = ((0 + g_0[i]) + g_1[i]) + ... + g_{P-1}[i];   g = g / P
+ *   bc1 = fp32(1 - beta1^t), bc2 = fp32(1 - beta2^t)   (host, in double)
+ *   mode 0: m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g);  mh = m/bc1;  vh = v/bc2
+ *   mode 1: m = (b1*m + (1-b1)*g)/bc1;  v = (b2*v + (1-b2)*(g*g))/bc2;  mh = m;  vh = v
+ *   mode 2: with bp = fp32(1 - beta^(t-1)):
+ *           m = (b1*(m*bp1) + (1-b1)*g)/bc1;  v = (b2*(v*bp2) + (1-b2)*(g*g))/bc2
+ *   master = master - lr * (mh / (sqrt(vh) + eps));  params[i] = fp16_rne(master)
+ *
+ * Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_EOVERLAP (any two of master, m, v,
+ * params overlap, or one of them overlaps the gradient span), ZERO_ECUDA.
+ * The grids never wait on anything: the call cannot hang the GPU. */
+int zero_adam_step(const void* grads_fp16, int64_t rank_stride, float* master, float* m,
+                   float* v, void* params_fp16, int64_t N, int32_t P, int32_t stage,
+                   int64_t t, float lr, float beta1, float beta2, float eps, int32_t mode,
+                   void* cuda_stream);
+
+/* One rank's part of the step: shard k = [min(kM,N), min((k+1)M,N)) of
+ * length len_k, M = ceil(N/P) ([P1] §（四） 第二步..第五步).
+ *
+ *  grads_fp16   device fp16: rank r's gradient for the shard's first element
+ *               is at element grad_offset + r * rank_stride.  Full per-rank
+ *               gradients: grad_offset = k*M, rank_stride >= N.  A packed
+ *               receive buffer [P][stride] of the shard only: grad_offset = 0,
+ *               rank_stride >= len_k.
+ *  master_s, m_s, v_s   device fp32 [len_k], the shard's state (for full
+ *               vectors pass master + k*M etc.).
+ *  params_out   device fp16 [len_k]: where shard k's new fp16 weights go --
+ *               params + k*M for the all-gathered vector (stages 0-2), or a
+ *               shard-local buffer (stage 3 keeps only its own shard).
+ *  The other arguments are as for zero_adam_step.  An empty shard
+ *  (len_k == 0) returns ZERO_OK without launching anything.
+ * The concatenation over k = 0..P-1 of the shard calls equals
+ * zero_adam_step bit for bit. */
+int zero_adam_step_shard(const void* grads_fp16, int64_t rank_stride, int64_t grad_offset,
+                         int32_t k, float* master_s, float* m_s, float* v_s,
+                         void* params_out, int64_t N, int32_t P, int32_t stage, int64_t t,
+                         float lr, float beta1, float beta2, float eps, int32_t mode,
+                         void* cuda_stream);
+
+/* Text of a status code (static storage; never NULL). */
+const char* zero_strerror(int code);
+
+/* The cudaError_t of the most recent ZERO_ECUDA on this thread (0 if none),
+ * and its name from the CUDA runtime. */
+int zero_last_cuda_error(void);
+const char* zero_last_cuda_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_STEP_H */

@@ -1,0 +1,102 @@
+"""The C ABI without a GPU: the library loads, exports every function its
+header declares, and rejects bad arguments on the host before any CUDA call.
+
+The rejection cases pass made-up device addresses; they run only where no
+GPU is visible, so a case that wrongly passed validation could never reach a
+kernel.  The same checks with real device buffers are in the GPU tests."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from conftest import cuda_available
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(zero_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_header_declares_the_step_api():
+    names = declared_functions()
+    assert {"zero_init_layout", "zero_free_layout", "zero_memory_bytes", "zero_adam_step",
+            "zero_adam_step_shard", "zero_strerror"} <= names
+
+
+def test_library_exports_every_declared_symbol(zlib):
+    L = zlib.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert set(zlib.EXPORTED) == declared_functions()
+
+
+def test_status_codes_match_header(zlib):
+    text = "".join(open(h).read() for h in HEADERS)
+    for name in ("ZERO_OK", "ZERO_EINVAL", "ZERO_EALIGN", "ZERO_EOVERLAP", "ZERO_ECUDA",
+                 "ZERO_ENOMEM", "ZERO_MAX_RANKS"):
+        m = re.search(r"#define\s+%s\s+\(?(-?\d+)\)?" % name, text)
+        assert m and int(m.group(1)) == getattr(zlib, name), name
+    for code in (0, -1, -2, -3, -4, -5):
+        assert zlib.zero_strerror(code)
+    assert "unknown" in zlib.zero_strerror(-99)
+
+
+no_gpu = pytest.mark.skipif(cuda_available(), reason="made-up device addresses: CPU-only check")
+
+A = 1 << 40                    # made-up, 256-byte aligned addresses, far apart
+G, W, MM, V, PP = A, 2 * A, 3 * A, 4 * A, 5 * A
+GOOD = dict(grads=G, rank_stride=1000, master=W, m=MM, v=V, params=PP, N=1000, P=4, stage=2,
+            t=1, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, mode=0)
+
+
+def _call(zlib, **kw):
+    a = dict(GOOD, **kw)
+    return zlib.lib().zero_adam_step(a["grads"], a["rank_stride"], a["master"], a["m"], a["v"],
+                                     a["params"], a["N"], a["P"], a["stage"], a["t"], a["lr"],
+                                     a["beta1"], a["beta2"], a["eps"], a["mode"], 0)
+
+
+@no_gpu
+@pytest.mark.parametrize("kw,code", [
+    (dict(grads=None), -1), (dict(master=None), -1), (dict(m=None), -1), (dict(v=None), -1),
+    (dict(params=None), -1), (dict(N=0), -1), (dict(N=-5), -1), (dict(P=0), -1),
+    (dict(P=1025), -1), (dict(stage=4), -1), (dict(stage=-1), -1), (dict(mode=3), -1),
+    (dict(mode=-1), -1), (dict(t=0), -1), (dict(lr=math.nan), -1), (dict(lr=math.inf), -1),
+    (dict(beta1=1.0), -1), (dict(beta2=-0.5), -1), (dict(eps=-1e-8), -1),
+    (dict(eps=math.inf), -1), (dict(rank_stride=999), -1),
+    (dict(master=W + 2), -2), (dict(v=V + 1), -2), (dict(params=PP + 1), -2),
+    (dict(grads=G + 1), -2),
+    (dict(m=W + 3996), -3), (dict(v=MM), -3), (dict(params=W + 100), -3),
+    (dict(master=G + 2 * 3000), -3), (dict(params=G + 2 * 3999), -3),
+])
+def test_step_rejects(zlib, kw, code):
+    assert _call(zlib, **kw) == code
+
+
+@no_gpu
+def test_shard_rejects_and_empty_shard(zlib):
+    L = zlib.lib()
+
+    def shard(k=0, off=0, N=1000, P=4, stride=250, w=W, m=MM, v=V, p=PP, g=G):
+        return L.zero_adam_step_shard(g, stride, off, k, w, m, v, p, N, P, 2, 1, 1e-3, 0.9,
+                                      0.999, 1e-8, 0, 0)
+
+    assert shard(k=4) == -1
+    assert shard(k=-1) == -1
+    assert shard(off=-1) == -1
+    assert shard(stride=249) == -1          # rank slices would overlap
+    assert shard(g=None) == -1
+    assert shard(w=W + 1) == -2
+    assert shard(p=W) == -3
+    # N = 5, P = 4: shard 3 owns nothing, returns success without any CUDA call
+    assert shard(k=3, N=5, stride=2) == 0

@@ -1,0 +1,196 @@
+"""Python binding of the fused ZeRO step library (``libzero_step.so``).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels (or, for the layout table, in its host C++).  The functions carry the
+C-ABI's names; tensors are torch tensors on the current CUDA device (or raw
+integer addresses), streams are torch streams (default: the current one).
+
+The library is built in-tree by :func:`build` (nvcc, sm_103a).  There is no
+fallback: if the library is missing, :func:`lib` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB as _LIB_PATH
+from ._build import build  # noqa: F401  (re-export)
+
+ZERO_OK = 0
+ZERO_EINVAL = -1
+ZERO_EALIGN = -2
+ZERO_EOVERLAP = -3
+ZERO_ECUDA = -4
+ZERO_ENOMEM = -5
+ZERO_MAX_RANKS = 1024
+
+MODE_STANDARD = 0
+MODE_FOLDED_LITERAL = 1
+MODE_FOLDED_STORAGE = 2
+
+# every symbol include/zero_step.h declares
+EXPORTED = ("zero_init_layout", "zero_free_layout", "zero_shard_range", "zero_memory_bytes",
+            "zero_adam_step", "zero_adam_step_shard", "zero_strerror",
+            "zero_last_cuda_error", "zero_last_cuda_error_string")
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        msg = f"{what}: {_strerror(code)} (status {code})"
+        if code == ZERO_ECUDA:
+            msg += f" [{lib().zero_last_cuda_error_string().decode()}]"
+        super().__init__(msg)
+        self.code = code
+
+
+class zero_segment_t(ctypes.Structure):
+    _fields_ = [("tensor_id", ctypes.c_int64), ("tensor_offset", ctypes.c_int64),
+                ("shard_offset", ctypes.c_int64), ("len", ctypes.c_int64)]
+
+
+class zero_layout_t(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("M", ctypes.c_int64), ("P", ctypes.c_int32),
+                ("stage", ctypes.c_int32), ("n_tensors", ctypes.c_int32),
+                ("reserved", ctypes.c_int32),
+                ("shard_begin", ctypes.POINTER(ctypes.c_int64)),
+                ("shard_end", ctypes.POINTER(ctypes.c_int64)),
+                ("seg_offsets", ctypes.POINTER(ctypes.c_int64)),
+                ("segs", ctypes.POINTER(zero_segment_t)),
+                ("n_segs", ctypes.c_int64),
+                ("bytes_per_rank_mixed", ctypes.c_double),
+                ("floats_per_rank_p1", ctypes.c_double),
+                ("comm_elems_per_rank", ctypes.c_double)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                           "zero_sharded_mixed_shard_gb300.build() (needs nvcc)")
+    L = ctypes.CDLL(_LIB_PATH)
+    i64, i32, f32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
+    L.zero_init_layout.argtypes = [ctypes.POINTER(ctypes.c_int64), i32, i32, i32,
+                                   ctypes.POINTER(zero_layout_t)]
+    L.zero_init_layout.restype = ctypes.c_int
+    L.zero_free_layout.argtypes = [ctypes.POINTER(zero_layout_t)]
+    L.zero_free_layout.restype = None
+    L.zero_shard_range.argtypes = [i64, i32, i32, ctypes.POINTER(ctypes.c_int64),
+                                   ctypes.POINTER(ctypes.c_int64)]
+    L.zero_shard_range.restype = ctypes.c_int
+    L.zero_memory_bytes.argtypes = [i64, i32, i32, ctypes.POINTER(ctypes.c_double),
+                                    ctypes.POINTER(ctypes.c_double),
+                                    ctypes.POINTER(ctypes.c_double)]
+    L.zero_memory_bytes.restype = ctypes.c_int
+    L.zero_adam_step.argtypes = [vp, i64, vp, vp, vp, vp, i64, i32, i32, i64,
+                                 f32, f32, f32, f32, i32, vp]
+    L.zero_adam_step.restype = ctypes.c_int
+    L.zero_adam_step_shard.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp, i64, i32, i32, i64,
+                                       f32, f32, f32, f32, i32, vp]
+    L.zero_adam_step_shard.restype = ctypes.c_int
+    L.zero_strerror.argtypes = [ctypes.c_int]
+    L.zero_strerror.restype = ctypes.c_char_p
+    L.zero_last_cuda_error.argtypes = []
+    L.zero_last_cuda_error.restype = ctypes.c_int
+    L.zero_last_cuda_error_string.argtypes = []
+    L.zero_last_cuda_error_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _strerror(code: int) -> str:
+    return lib().zero_strerror(code).decode()
+
+
+def zero_strerror(code: int) -> str:
+    return _strerror(code)
+
+
+def _addr(x) -> int | None:
+    """Device address of a tensor (or pass an int / None through)."""
+    if x is None or isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def zero_shard_range(N: int, P: int, k: int) -> tuple[int, int]:
+    b, e = ctypes.c_int64(), ctypes.c_int64()
+    rc = lib().zero_shard_range(N, P, k, ctypes.byref(b), ctypes.byref(e))
+    if rc:
+        raise ZeroError(rc, "zero_shard_range")
+    return b.value, e.value
+
+
+def zero_memory_bytes(N: int, P: int, stage: int) -> tuple[float, float, float]:
+    """(model-state bytes per rank, float count per rank, elements moved per rank)."""
+    b, f, c = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    rc = lib().zero_memory_bytes(N, P, stage, ctypes.byref(b), ctypes.byref(f), ctypes.byref(c))
+    if rc:
+        raise ZeroError(rc, "zero_memory_bytes")
+    return b.value, f.value, c.value
+
+
+def zero_init_layout(tensor_numel, P: int, stage: int) -> dict:
+    """Layout table as plain Python data (the C table is freed before
+    returning): N, M, P, stage, shard bounds, per-shard segments and the
+    accounting figures."""
+    n = len(tensor_numel)
+    arr = (ctypes.c_int64 * max(n, 1))(*tensor_numel)
+    t = zero_layout_t()
+    rc = lib().zero_init_layout(arr, n, P, stage, ctypes.byref(t))
+    if rc:
+        raise ZeroError(rc, "zero_init_layout")
+    try:
+        segs = []
+        for k in range(t.P):
+            lo, hi = t.seg_offsets[k], t.seg_offsets[k + 1]
+            segs.append([(t.segs[j].tensor_id, t.segs[j].tensor_offset,
+                          t.segs[j].shard_offset, t.segs[j].len) for j in range(lo, hi)])
+        return {
+            "N": t.N, "M": t.M, "P": t.P, "stage": t.stage,
+            "shards": [(t.shard_begin[k], t.shard_end[k]) for k in range(t.P)],
+            "segments": segs,
+            "n_segs": t.n_segs,
+            "bytes_per_rank_mixed": t.bytes_per_rank_mixed,
+            "floats_per_rank_p1": t.floats_per_rank_p1,
+            "comm_elems_per_rank": t.comm_elems_per_rank,
+        }
+    finally:
+        lib().zero_free_layout(ctypes.byref(t))
+
+
+def zero_adam_step(grads, rank_stride: int, master, m, v, params, N: int, P: int, stage: int,
+                   t: int, lr: float, beta1: float, beta2: float, eps: float, mode: int,
+                   stream=None) -> None:
+    """Enqueue one whole-vector ZeRO step (see include/zero_step.h)."""
+    rc = lib().zero_adam_step(_addr(grads), rank_stride, _addr(master), _addr(m), _addr(v),
+                              _addr(params), N, P, stage, t, lr, beta1, beta2, eps, mode,
+                              _stream(stream))
+    if rc:
+        raise ZeroError(rc, "zero_adam_step")
+
+
+def zero_adam_step_shard(grads, rank_stride: int, grad_offset: int, k: int, master_s, m_s,
+                         v_s, params_out, N: int, P: int, stage: int, t: int, lr: float,
+                         beta1: float, beta2: float, eps: float, mode: int,
+                         stream=None) -> None:
+    """Enqueue shard k's step (see include/zero_step.h)."""
+    rc = lib().zero_adam_step_shard(_addr(grads), rank_stride, grad_offset, k, _addr(master_s),
+                                    _addr(m_s), _addr(v_s), _addr(params_out), N, P, stage, t,
+                                    lr, beta1, beta2, eps, mode, _stream(stream))
+    if rc:
+        raise ZeroError(rc, "zero_adam_step_shard")

@@ -155,23 +155,29 @@ def np_state(n: int, seed: int, master_sigma: float = 0.02):
 
 def torch_grads(P: int, n: int, stride: int, sigma: float, seed: int, device,
                 heavy_tail_frac: float = 0.0, zero_frac: float = 0.0,
-                step: int = 0):
+                step: int = 0, out=None):
     """fp16 gradients [P, stride] on ``device`` (padding entries 0), drawn
     rank by rank from a seeded device generator.  ``step`` selects a fresh
-    draw for a later step of the same workload."""
+    draw for a later step of the same workload; ``out`` reuses a buffer."""
     import torch
     gen = torch.Generator(device=device)
     gen.manual_seed(seed * 1_000_003 + step)
-    out = torch.zeros((P, stride), dtype=torch.float16, device=device)
+    if out is None:
+        out = torch.zeros((P, stride), dtype=torch.float16, device=device)
+    else:
+        assert out.shape == (P, stride) and out.dtype == torch.float16
+        out[:, n:].zero_()
     for r in range(P):
         x = torch.randn(n, generator=gen, device=device, dtype=torch.float32)
         x.mul_(sigma)
         if heavy_tail_frac:
             sel = torch.rand(n, generator=gen, device=device) < heavy_tail_frac
             x[sel] *= 100.0
+            del sel
         if zero_frac:
             sel = torch.rand(n, generator=gen, device=device) < zero_frac
             x[sel] = 0.0
+            del sel
         out[r, :n].copy_(x)
         del x
     return out
