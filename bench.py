@@ -138,24 +138,34 @@ class ClockSampler:
             self.proc.kill()
         self.out.flush()
         self.out.seek(0)
-        rows = []
-        for line in self.out.read().splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
-                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
-                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
-            except (ValueError, IndexError):
-                continue
+        text = self.out.read()
+        self.out.close()
         os.unlink(self.out.name)
-        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = sorted({names[i] for r in inside for i, s in enumerate(r[3]) if s == "Active"})
-        return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
-                "sm_max_mhz": max((r[2] for r in inside), default=None),
-                "reasons": reasons, "samples": len(inside)}
+        return parse_clock_csv(text, t0, t1)
+
+
+def parse_clock_csv(text: str, t0: float, t1: float) -> dict:
+    """Median SM clock, max clock and active slowdown reasons of the samples
+    taken between host times t0 and t1 (nvidia-smi's local timestamps)."""
+    rows = []
+    for line in text.splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            stamp = parts[0]
+            ts = time.mktime(time.strptime(stamp.split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            if "." in stamp:
+                ts += float("0." + stamp.split(".")[1])
+            rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+        except (ValueError, IndexError):
+            continue
+    inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+    names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    reasons = sorted({names[i] for r in inside for i, s in enumerate(r[3]) if s == "Active"})
+    return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
+            "sm_max_mhz": max((r[2] for r in inside), default=None),
+            "reasons": reasons, "samples": len(inside)}
 
 
 # ---------------------------------------------------------------------------

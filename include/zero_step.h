@@ -185,7 +185,9 @@ int zero_adam_step(const void* grads_fp16, int64_t rank_stride, float* master, f
  *               params + k*M for the all-gathered vector (stages 0-2), or a
  *               shard-local buffer (stage 3 keeps only its own shard).
  *  The other arguments are as for zero_adam_step.  An empty shard
- *  (len_k == 0) returns ZERO_OK without launching anything.
+ *  (len_k == 0) returns ZERO_OK without launching anything and without
+ *  examining the buffer pointers (they may be NULL); the scalar arguments
+ *  are still validated.
  * The concatenation over k = 0..P-1 of the shard calls equals
  * zero_adam_step bit for bit. */
 int zero_adam_step_shard(const void* grads_fp16, int64_t rank_stride, int64_t grad_offset,

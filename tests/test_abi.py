@@ -98,5 +98,9 @@ def test_shard_rejects_and_empty_shard(zlib):
     assert shard(g=None) == -1
     assert shard(w=W + 1) == -2
     assert shard(p=W) == -3
-    # N = 5, P = 4: shard 3 owns nothing, returns success without any CUDA call
+    # N = 5, P = 4: shard 3 owns nothing, returns success without any CUDA call,
+    # even with no buffers at all; its scalars are still checked
     assert shard(k=3, N=5, stride=2) == 0
+    assert shard(k=3, N=5, stride=2, g=None, w=None, m=None, v=None, p=None) == 0
+    assert L.zero_adam_step_shard(None, 2, 0, 3, None, None, None, None, 5, 4, 2, 0, 1e-3, 0.9,
+                                  0.999, 1e-8, 0, 0) == -1   # t = 0

@@ -1,0 +1,84 @@
+"""Host logic of bench.py without a GPU: argument defaults, the clock-log
+parser, the profile lookup, and the multi-process path (barrier and the
+max over ranks) as two gloo ranks on CPU."""
+import os
+import socket
+import sys
+import time
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_defaults():
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.workload == "gpt2s" and a.warmup >= 3 and a.steps >= 100
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--warmup", "2"])
+
+
+def test_clock_parser_keeps_samples_of_the_timed_region():
+    t0 = time.mktime(time.strptime("2026/12/02 08:00:01", "%Y/%m/%d %H:%M:%S"))
+    lines = [
+        "2026/12/02 08:00:00.500, 0, 900, 2070, 200.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 08:00:01.100, 0, 1900, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 08:00:01.300, 0, 1950, 2070, 950.5, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 08:00:01.500, 0, 2000, 2070, 990.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+        "2026/12/02 08:00:03.000, 0, 800, 2070, 150.0, 0x0, Active, Not Active, Not Active, Not Active",
+    ]
+    c = bench.parse_clock_csv("\n".join(lines), t0, t0 + 0.6)
+    assert c["samples"] == 3 and c["sm_mhz"] == 1950 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"]
+
+
+def test_profile_traffic_requires_matching_source(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "PROFILE_DIR", str(tmp_path))
+    f = tmp_path / "zero_fused_step_gpt2s.txt"
+    f.write_text(f"source_sha256: {bench.kernel_source_hash()}\ntraffic_bytes_per_launch: 123\n")
+    assert bench.profiled_traffic("gpt2s") == 123.0
+    f.write_text("source_sha256: 0000\ntraffic_bytes_per_launch: 123\n")
+    assert bench.profiled_traffic("gpt2s") is None
+    assert bench.profiled_traffic("tiny") is None
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world),
+                      RANK=str(rank), LOCAL_RANK=str(rank))
+    d = bench.Dist()
+    d.init("gloo")
+    d.barrier()
+    got = d.max(10.0 + rank)
+    d.barrier()
+    out.put((rank, d.world, got))
+    d.close()
+
+
+def test_two_gloo_ranks_take_the_slowest_time():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == [(0, 2, 11.0), (1, 2, 11.0)]
+
+
+def test_reference_arm_other_ranks_do_no_work(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3"]) == 0

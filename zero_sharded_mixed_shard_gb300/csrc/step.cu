@@ -464,8 +464,10 @@ extern "C" int zero_adam_step_shard(const void* grads_fp16, int64_t rank_stride,
     const int64_t b = static_cast<int64_t>(k) * M < N ? static_cast<int64_t>(k) * M : N;
     const int64_t e = b + M < N ? b + M : N;
     const int64_t len = e - b;
+    // a trailing rank that owns nothing: no buffer is touched, so none is
+    // examined (zero-length allocations are often NULL)
+    if (len == 0) return ZERO_OK;
     if (!grads_fp16 || !master_s || !m_s || !v_s || !params_out) return ZERO_EINVAL;
-    if (len == 0) return ZERO_OK; // a trailing rank that owns nothing
     StepArgs a{};
     a.g = static_cast<const __half*>(grads_fp16) + grad_offset;
     a.stride = rank_stride;
