@@ -380,7 +380,7 @@ def run_ours(args, wl, mode, dist):
             "pct_of_nominal_8tbs": 100 * alg_bytes * K / (region_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "zero_fused_step_kernel",
+                         "kernel": "zero_fused_step_tma_kernel",
                          "peak_kind": f"{peak_kind} HBM copy bandwidth",
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "mean_launch_ms": mean_launch_ms},

@@ -196,6 +196,33 @@ int zero_adam_step_shard(const void* grads_fp16, int64_t rank_stride, int64_t gr
                          float lr, float beta1, float beta2, float eps, int32_t mode,
                          void* cuda_stream);
 
+/* Bounded waits that gave up, over every step launched on the current
+ * device since the last reset.  The fused kernels wait on shared-memory
+ * barriers for their own bulk copies; each wait gives up after 2 seconds,
+ * lets the copies already issued land, counts itself here and returns, so
+ * a stuck copy can never hang the GPU.  The count is 0 in every correct run;
+ * a non-zero count means the outputs of some step are incomplete.
+ * Reading it synchronises with the current device (cudaMemcpyFromSymbol);
+ * reset != 0 sets it back to 0.  Errors: ZERO_EINVAL (count NULL),
+ * ZERO_ECUDA. */
+int zero_device_timeouts(int64_t* count, int32_t reset);
+
+/* Diagnostic of the bounded waits (no counterpart on the pages): enqueues
+ * the step of zero_adam_step (same arguments) through the bulk-copy kernel
+ * with one shared-memory barrier of its first CTA told to expect 16 bytes
+ * that no copy delivers.  That CTA's wait runs out after 2 seconds, it lets
+ * its other copies land (the poisoned wait runs out once more), adds 1 to
+ * the count of zero_device_timeouts and returns; every other CTA finishes
+ * normally and the context stays usable.  The first CTA's tiles are left
+ * partly updated, so the buffers hold no valid step afterwards.  Takes
+ * about 4 s of GPU time.  Errors: as zero_adam_step, and ZERO_EINVAL when
+ * the problem does not take the bulk-copy path (buffers on different 16-byte
+ * phases, or fewer 2048-element tiles than SMs). */
+int zero_selftest_wait_timeout(const void* grads_fp16, int64_t rank_stride, float* master, float* m,
+                               float* v, void* params_fp16, int64_t N, int32_t P, int32_t stage,
+                               int64_t t, float lr, float beta1, float beta2, float eps,
+                               int32_t mode, void* cuda_stream);
+
 /* Text of a status code (static storage; never NULL). */
 const char* zero_strerror(int code);
 

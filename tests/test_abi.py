@@ -81,6 +81,11 @@ def _call(zlib, **kw):
 ])
 def test_step_rejects(zlib, kw, code):
     assert _call(zlib, **kw) == code
+    # the diagnostic entry point validates exactly like the step
+    a = dict(GOOD, **kw)
+    assert zlib.lib().zero_selftest_wait_timeout(
+        a["grads"], a["rank_stride"], a["master"], a["m"], a["v"], a["params"], a["N"], a["P"],
+        a["stage"], a["t"], a["lr"], a["beta1"], a["beta2"], a["eps"], a["mode"], 0) == code
 
 
 @no_gpu

@@ -120,6 +120,39 @@ def test_special_values(z):
             assert_close(host_state(s), ref + [p_ref], f"mode={mode} t={t}")
 
 
+@pytest.mark.parametrize("big", [False, True])
+def test_special_state_values(z, big):
+    """master / m / v holding +-inf, NaN, +-0, huge and tiny values (on both
+    the vector path and the bulk pipeline): infinities and NaN go through the
+    divides and the square root exactly as IEEE 754 says, on both sides."""
+    P = 4
+    N = (torch.cuda.get_device_properties(0).multi_processor_count * 2048 * 4 + 8) if big else 4096
+    rng = np.random.default_rng(8)
+    codes = synth.np_grads(P, N, N, 1e-3, 8)
+    specials = np.array([np.inf, -np.inf, np.nan, 0.0, -0.0, 3e38, -3e38, 1e-45, 1e-38, 1.0],
+                        np.float32)
+
+    def sprinkle(x):
+        # specials only in [N/3, N/2): on the bulk pipeline the warps that
+        # hold one take the guarded branch, all others the plain one
+        pick = rng.random(N) < 0.3
+        pick[: N // 3] = False
+        pick[N // 2:] = False
+        x[pick] = rng.choice(specials, size=int(pick.sum()))
+        return x
+
+    w0 = sprinkle(rng.standard_normal(N).astype(np.float32))
+    m0 = sprinkle((rng.standard_normal(N) * 1e-3).astype(np.float32))
+    v0 = sprinkle((rng.random(N) * 1e-6).astype(np.float32))
+    for mode in (0, 1, 2):
+        for t in (1, 3):
+            ref = [w0.copy(), m0.copy(), v0.copy()]
+            s = dev_state(w0, m0, v0, np.zeros(N, np.uint16))
+            gpu_step(z, dev_u16(codes), N, s, N, P, t, mode)
+            p_ref = oracle.adam_elems(codes, N, P, *ref, t, LR, B1, B2, EPS, mode, threads=8)
+            assert_close(host_state(s), ref + [p_ref], f"mode={mode} t={t} big={big}")
+
+
 @pytest.mark.parametrize("stride", [10_004, 10_008])
 @pytest.mark.parametrize("offs", [(0, 0, 0, 0, 0), (3, 3, 3, 3, 3), (1, 1, 1, 1, 1),
                                   (0, 4, 0, 0, 0), (2, 0, 2, 2, 0), (5, 1, 7, 3, 2),
@@ -283,4 +316,78 @@ def test_validation_with_device_buffers(z):
     assert e.value.code == z.ZERO_EALIGN
     torch.cuda.synchronize()
     for x, y in zip(host_state(s), before):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+# ---------------------------------------------------------------------------
+# the bulk-copy pipeline: large enough that every SM gets tiles of 2048
+# ---------------------------------------------------------------------------
+
+def _tma_size(extra):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return sms * 2048 * 2 + extra
+
+
+@pytest.mark.parametrize("P", [1, 3, 4, 8, 13, 16, 33, 64])
+def test_tma_path_matches_oracle(z, P):
+    """P that fills whole 8-rank chunks and P that leaves a partial last chunk;
+    a ragged tail of 5 elements; three steps of every mode."""
+    N = _tma_size(4101)            # 512 full tiles on 152 SMs, a partial tile, a tail of 5
+    stride = synth.round_up(N, 8) + 8
+    worst = (0, 0)
+    for mode in (0, 1, 2):
+        w0, m0, v0, p0 = synth.np_state(N, 70 + P)
+        ref = [w0.copy(), m0.copy(), v0.copy()]
+        s = dev_state(w0, m0, v0, p0)
+        for t in range(1, 4):
+            codes = synth.np_grads(P, N, stride, 1e-3, 300 * t + P, heavy_tail_frac=0.01,
+                                   zero_frac=0.05)
+            gpu_step(z, dev_u16(codes), stride, s, N, P, t, mode)
+            p_ref = oracle.adam_elems(codes, stride, P, *ref, t, LR, B1, B2, EPS, mode, threads=8)
+            u = max_ulps(host_state(s), ref + [p_ref])
+            worst = (max(worst[0], u[0]), max(worst[1], u[1]))
+    assert worst == (0, 0), f"P={P}: max ulp {worst}"
+    assert z.zero_device_timeouts() == 0
+
+
+@pytest.mark.parametrize("head", [1, 3, 7])
+def test_tma_path_with_head(z, head):
+    """Every buffer starts `head` elements past a 16-byte boundary: the first
+    8 - head elements are done one by one, the rest by the bulk pipeline."""
+    P, N = 8, _tma_size(777)
+    stride = synth.round_up(N + head, 8)
+    codes = synth.np_grads(P, N, stride, 1e-3, 91 + head)
+    g_buf = torch.zeros(P * stride + 8, dtype=torch.int16, device="cuda")
+    g_buf[head: head + P * stride] = torch.from_numpy(codes.view(np.int16)).cuda()
+    g = g_buf.view(torch.float16)[head:]
+    w0, m0, v0, _ = synth.np_state(N, 5)
+    bufs = []
+    for arr in (w0, m0, v0):
+        b = torch.zeros(N + 8, dtype=torch.float32, device="cuda")
+        b[head: head + N] = torch.from_numpy(arr).cuda()
+        bufs.append(b[head: head + N])
+    p_buf = torch.zeros(N + 8, dtype=torch.int16, device="cuda")
+    params = p_buf.view(torch.float16)[head: head + N]
+    z.zero_adam_step(g, stride, *bufs, params, N, P, 2, 1, LR, B1, B2, EPS, 0)
+    ref = [w0.copy(), m0.copy(), v0.copy()]
+    p_ref = oracle.adam_elems(codes, stride, P, *ref, 1, LR, B1, B2, EPS, 0, threads=8)
+    assert max_ulps(host_state(bufs + [params]), ref + [p_ref]) == (0, 0)
+
+
+def test_tma_and_vector_paths_agree(z):
+    """The same problem through the bulk pipeline (aligned buffers) and the
+    vector path (fp16 output one element off the gradients' phase) gives the
+    same bytes."""
+    P, N = 16, _tma_size(123)
+    stride = synth.round_up(N, 8)
+    codes = synth.np_grads(P, N, stride, 1e-3, 4)
+    g = dev_u16(codes)
+    w0, m0, v0, p0 = synth.np_state(N, 4)
+    a = dev_state(w0, m0, v0, p0)
+    gpu_step(z, g, stride, a, N, P, 2, 0)
+    b = dev_state(w0, m0, v0, p0)
+    p_buf = torch.zeros(N + 1, dtype=torch.int16, device="cuda")
+    b[3] = p_buf.view(torch.float16)[1:]
+    gpu_step(z, g, stride, b, N, P, 2, 0)
+    for x, y in zip(host_state(a), host_state(b)):
         assert np.array_equal(x.view(np.uint8), y.view(np.uint8))

@@ -30,7 +30,8 @@ MODE_FOLDED_STORAGE = 2
 
 # every symbol include/zero_step.h declares
 EXPORTED = ("zero_init_layout", "zero_free_layout", "zero_shard_range", "zero_memory_bytes",
-            "zero_adam_step", "zero_adam_step_shard", "zero_strerror",
+            "zero_adam_step", "zero_adam_step_shard", "zero_device_timeouts",
+            "zero_selftest_wait_timeout", "zero_strerror",
             "zero_last_cuda_error", "zero_last_cuda_error_string")
 
 
@@ -93,6 +94,11 @@ def lib() -> ctypes.CDLL:
     L.zero_adam_step_shard.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp, i64, i32, i32, i64,
                                        f32, f32, f32, f32, i32, vp]
     L.zero_adam_step_shard.restype = ctypes.c_int
+    L.zero_selftest_wait_timeout.argtypes = [vp, i64, vp, vp, vp, vp, i64, i32, i32, i64,
+                                             f32, f32, f32, f32, i32, vp]
+    L.zero_selftest_wait_timeout.restype = ctypes.c_int
+    L.zero_device_timeouts.argtypes = [ctypes.POINTER(ctypes.c_int64), i32]
+    L.zero_device_timeouts.restype = ctypes.c_int
     L.zero_strerror.argtypes = [ctypes.c_int]
     L.zero_strerror.restype = ctypes.c_char_p
     L.zero_last_cuda_error.argtypes = []
@@ -194,3 +200,24 @@ def zero_adam_step_shard(grads, rank_stride: int, grad_offset: int, k: int, mast
                                     lr, beta1, beta2, eps, mode, _stream(stream))
     if rc:
         raise ZeroError(rc, "zero_adam_step_shard")
+
+
+def zero_device_timeouts(reset: bool = False) -> int:
+    """Bounded waits that gave up on the current device (0 in a correct run);
+    synchronises with the device."""
+    n = ctypes.c_int64()
+    rc = lib().zero_device_timeouts(ctypes.byref(n), 1 if reset else 0)
+    if rc:
+        raise ZeroError(rc, "zero_device_timeouts")
+    return n.value
+
+
+def zero_selftest_wait_timeout(grads, rank_stride: int, master, m, v, params, N: int, P: int,
+                               stage: int, t: int, lr: float, beta1: float, beta2: float,
+                               eps: float, mode: int, stream=None) -> None:
+    """Enqueue the bounded-wait diagnostic (see include/zero_step.h)."""
+    rc = lib().zero_selftest_wait_timeout(_addr(grads), rank_stride, _addr(master), _addr(m),
+                                          _addr(v), _addr(params), N, P, stage, t, lr, beta1,
+                                          beta2, eps, mode, _stream(stream))
+    if rc:
+        raise ZeroError(rc, "zero_selftest_wait_timeout")

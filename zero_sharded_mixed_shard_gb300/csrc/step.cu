@@ -27,6 +27,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "zero_step.h"
 
@@ -50,6 +51,7 @@ struct StepArgs {
     int p_pow2;         // P is a power of two: g * (1/P) == g / P exactly
     float inv_p;        // 1/P (exact when p_pow2)
     float lr, b1, b2, omb1, omb2, bc1, bc2, bp1, bp2, eps;
+    unsigned int poison_tx; // diagnostic only: extra bytes CTA 0's first barrier expects (0 otherwise)
 };
 
 // ---------------------------------------------------------------------------
@@ -66,8 +68,41 @@ __device__ __forceinline__ float finish_mean(float sum, const StepArgs& a)
     }
 }
 
-// Adam on one element; w, m, v updated in place, returns the new master.
-template <int MODE>
+// IEEE quotients whose operands are infinite are formed directly: CUDA's
+// correctly rounded divide and square root send such operands down a slow
+// path, and once the literal folded reading overflows v every element would
+// take it.  The results are the IEEE 754 ones.
+//   x / d for d positive and finite (the bias corrections): inf stays inf.
+template <int G>
+__device__ __forceinline__ float div_by_positive(float x, float d)
+{
+    if constexpr (G == 0) return __fdiv_rn(x, d);
+    return isinf(x) ? x : __fdiv_rn(x, d);
+}
+
+__device__ __forceinline__ bool is_pos_inf(float x) { return x == __int_as_float(0x7f800000); }
+
+//   sqrt(+inf) = +inf (every other input goes to the rounded square root).
+template <int G>
+__device__ __forceinline__ float sqrt_rn(float x)
+{
+    if constexpr (G == 0) return __fsqrt_rn(x);
+    return is_pos_inf(x) ? x : __fsqrt_rn(x);
+}
+
+//   x / +inf: a zero carrying x's sign for finite x, NaN for infinite or NaN x.
+template <int G>
+__device__ __forceinline__ float div_rn(float x, float d)
+{
+    if constexpr (G == 0) return __fdiv_rn(x, d);
+    if (is_pos_inf(d)) return isfinite(x) ? copysignf(0.0f, x) : __int_as_float(0x7fffffff);
+    return __fdiv_rn(x, d);
+}
+
+// Adam on one element; w, m, v updated in place.  G = 1 takes the shortcuts
+// above for infinite operands, G = 0 calls the rounded intrinsics directly
+// (same results; only the speed on infinite operands differs).
+template <int MODE, int G = 1>
 __device__ __forceinline__ void adam_elem(const StepArgs& a, float g, float& w, float& m, float& v)
 {
     const float gg = __fmul_rn(g, g);
@@ -75,21 +110,21 @@ __device__ __forceinline__ void adam_elem(const StepArgs& a, float g, float& w, 
     if constexpr (MODE == ZERO_MODE_STANDARD) {
         m_new = __fadd_rn(__fmul_rn(a.b1, m), __fmul_rn(a.omb1, g));
         v_new = __fadd_rn(__fmul_rn(a.b2, v), __fmul_rn(a.omb2, gg));
-        m_hat = __fdiv_rn(m_new, a.bc1);
-        v_hat = __fdiv_rn(v_new, a.bc2);
+        m_hat = div_by_positive<G>(m_new, a.bc1);
+        v_hat = div_by_positive<G>(v_new, a.bc2);
     } else if constexpr (MODE == ZERO_MODE_FOLDED_LITERAL) {
-        m_new = __fdiv_rn(__fadd_rn(__fmul_rn(a.b1, m), __fmul_rn(a.omb1, g)), a.bc1);
-        v_new = __fdiv_rn(__fadd_rn(__fmul_rn(a.b2, v), __fmul_rn(a.omb2, gg)), a.bc2);
+        m_new = div_by_positive<G>(__fadd_rn(__fmul_rn(a.b1, m), __fmul_rn(a.omb1, g)), a.bc1);
+        v_new = div_by_positive<G>(__fadd_rn(__fmul_rn(a.b2, v), __fmul_rn(a.omb2, gg)), a.bc2);
         m_hat = m_new;
         v_hat = v_new;
     } else {
-        m_new = __fdiv_rn(__fadd_rn(__fmul_rn(a.b1, __fmul_rn(m, a.bp1)), __fmul_rn(a.omb1, g)), a.bc1);
-        v_new = __fdiv_rn(__fadd_rn(__fmul_rn(a.b2, __fmul_rn(v, a.bp2)), __fmul_rn(a.omb2, gg)), a.bc2);
+        m_new = div_by_positive<G>(__fadd_rn(__fmul_rn(a.b1, __fmul_rn(m, a.bp1)), __fmul_rn(a.omb1, g)), a.bc1);
+        v_new = div_by_positive<G>(__fadd_rn(__fmul_rn(a.b2, __fmul_rn(v, a.bp2)), __fmul_rn(a.omb2, gg)), a.bc2);
         m_hat = m_new;
         v_hat = v_new;
     }
-    const float denom = __fadd_rn(__fsqrt_rn(v_hat), a.eps);
-    const float upd = __fdiv_rn(m_hat, denom);
+    const float denom = __fadd_rn(sqrt_rn<G>(v_hat), a.eps);
+    const float upd = div_rn<G>(m_hat, denom);
     w = __fsub_rn(w, __fmul_rn(a.lr, upd));
     m = m_new;
     v = v_new;
@@ -265,6 +300,248 @@ __global__ void __launch_bounds__(kThreads) zero_fused_step_kernel(const StepArg
 }
 
 // ---------------------------------------------------------------------------
+// TMA bulk-copy pipeline: the main path when every stream shares one 16-byte
+// phase.  One CTA per SM walks its tiles of kTile elements.  A unit of work is
+// (tile, chunk of kChunkRanks ranks): one bulk copy of kTile*2 bytes per rank
+// of the chunk, plus the tile's master / m / v rows with the first chunk, all
+// landing in one of kStages shared-memory stages and counted by that stage's
+// mbarrier.  One elected thread issues the copies; every thread then reads its
+// 8 elements of each row from shared memory, accumulates the chunk's ranks in
+// rank order, and after the last chunk runs Adam and stores the results with
+// 16-byte streaming stores.  Copies of whole 4 KB rows keep the copy engine's
+// issue rate far from the limit and keep every DRAM stream long and sequential.
+// ---------------------------------------------------------------------------
+
+constexpr int kTile = 2048;
+constexpr int kChunkRanks = 8;
+constexpr int kStages = 4;
+constexpr uint32_t kGradBytes = kChunkRanks * kTile * 2;          // 32 KB of gradient rows
+constexpr uint32_t kStageBytes = kGradBytes + 3 * kTile * 4;      // + 24 KB of fp32 state
+constexpr size_t kBulkSmem = size_t(kStages) * kStageBytes;       // 224 KB
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;        // a bounded wait gives up after 2 s
+
+// Bounded waits that gave up (0 in every correct run); read by zero_device_timeouts.
+__device__ unsigned int g_wait_timeouts;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done)
+                 : "r"(smem_addr(bar)), "r"(parity)
+                 : "memory");
+    return done != 0;
+}
+
+// Wait for the phase of `bar` with the given parity; false once kWaitLimitNs
+// have passed (and in any case after 2^20 rounds of 256 polls).
+__device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity)
+{
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (int round = 0; round < (1 << 20); ++round) {
+        for (int k = 0; k < 256; ++k)
+            if (mbar_test(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+                 : "memory");
+}
+
+// Smem reads of E consecutive halves / floats.
+template <int E>
+__device__ __forceinline__ HalfRaw<E> smem_halves(const unsigned char* p)
+{
+    HalfRaw<E> r;
+    if constexpr (E == 8) r.u = *reinterpret_cast<const uint4*>(p);
+    else if constexpr (E == 4) r.u = *reinterpret_cast<const uint2*>(p);
+    else r.u = *reinterpret_cast<const unsigned int*>(p);
+    return r;
+}
+
+template <int E>
+__device__ __forceinline__ void smem_floats(const unsigned char* p, float (&x)[E])
+{
+    if constexpr (E == 8) {
+        const float4 lo = reinterpret_cast<const float4*>(p)[0], hi = reinterpret_cast<const float4*>(p)[1];
+        x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+        x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
+    } else if constexpr (E == 4) {
+        const float4 lo = *reinterpret_cast<const float4*>(p);
+        x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+    } else {
+        const float2 lo = *reinterpret_cast<const float2*>(p);
+        x[0] = lo.x; x[1] = lo.y;
+    }
+}
+
+// NT consumer threads, E = kTile / NT consecutive elements each per tile.
+template <int MODE, int PT, int NT, int G>
+__global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepArgs a)
+{
+    constexpr int E = kTile / NT;
+    static_assert(E * NT == kTile && (E == 2 || E == 4 || E == 8), "tile split over the threads");
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ uint64_t full[kStages];
+
+    const int P = PT > 0 ? PT : a.P;
+    const int nch = (P + kChunkRanks - 1) / kChunkRanks;
+    const int tid = threadIdx.x;
+
+    // The bulk range is [head, head + nbulk), nbulk a multiple of 8 so every
+    // row copy is a multiple of 16 bytes; CTA 0 does the < 8 + < 8 ragged
+    // elements outside it one by one.
+    const long long nbulk = ((a.n - a.head) / 8) * 8;
+    const long long tail_start = a.head + nbulk;
+    if (blockIdx.x == 0) {
+        if (tid < a.head) step_elems<MODE, 1, PT>(a, tid);
+        if (tid < a.n - tail_start) step_elems<MODE, 1, PT>(a, tail_start + tid);
+    }
+    const long long ntiles = (nbulk + kTile - 1) / kTile;
+    const long long my_tiles = ntiles > blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const long long units = my_tiles * nch;
+    if (units == 0) return; // uniform over the CTA, before any barrier
+
+    uint64_t policy = 0;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    }
+    __syncthreads();
+
+    const __half* g0 = a.g + a.head;
+    float* w0 = a.w + a.head;
+    float* m0 = a.m + a.head;
+    float* v0 = a.v + a.head;
+    __half* p0 = a.p + a.head;
+
+    auto tile_of = [&](long long u) { return blockIdx.x + (u / nch) * gridDim.x; };
+    auto issue = [&](long long u) { // thread 0 only
+        const int s = static_cast<int>(u % kStages);
+        const int c = static_cast<int>(u % nch);
+        const long long i0 = tile_of(u) * kTile;
+        const long long len = nbulk - i0 < kTile ? nbulk - i0 : kTile;
+        const int rc = P - c * kChunkRanks < kChunkRanks ? P - c * kChunkRanks : kChunkRanks;
+        const uint32_t hb = static_cast<uint32_t>(len) * 2, fb = static_cast<uint32_t>(len) * 4;
+        unsigned char* st = smem + static_cast<size_t>(s) * kStageBytes;
+        const uint32_t poison = (u == 0 && blockIdx.x == 0) ? a.poison_tx : 0u;
+        mbar_arrive_expect_tx(&full[s], hb * rc + (c == 0 ? 3 * fb : 0) + poison);
+        const __half* src = g0 + static_cast<long long>(c) * kChunkRanks * a.stride + i0;
+        for (int q = 0; q < rc; ++q)
+            bulk_load(st + static_cast<size_t>(q) * kTile * 2, src + q * a.stride, hb, &full[s], policy);
+        if (c == 0) {
+            bulk_load(st + kGradBytes, w0 + i0, fb, &full[s], policy);
+            bulk_load(st + kGradBytes + kTile * 4, m0 + i0, fb, &full[s], policy);
+            bulk_load(st + kGradBytes + 2 * kTile * 4, v0 + i0, fb, &full[s], policy);
+        }
+    };
+
+    if (tid == 0)
+        for (long long u = 0; u < kStages && u < units; ++u) issue(u);
+
+    float acc[E], w[E], m[E], v[E];
+    long long u = 0;
+    bool failed = false;
+    for (; u < units; ++u) {
+        const int s = static_cast<int>(u % kStages);
+        const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>((u / kStages) & 1));
+        // one decision for the whole CTA; also: every thread is done with unit u-1
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        if (tid == 0 && u >= 1 && u - 1 + kStages < units) issue(u - 1 + kStages);
+
+        const int c = static_cast<int>(u % nch);
+        const long long i0 = tile_of(u) * kTile;
+        const long long len = nbulk - i0 < kTile ? nbulk - i0 : kTile;
+        const unsigned char* st = smem + static_cast<size_t>(s) * kStageBytes;
+        const int e0 = tid * E;
+        if (e0 < len) {
+            if (c == 0) {
+#pragma unroll
+                for (int j = 0; j < E; ++j) acc[j] = 0.0f;
+                smem_floats<E>(st + kGradBytes + e0 * 4, w);
+                smem_floats<E>(st + kGradBytes + kTile * 4 + e0 * 4, m);
+                smem_floats<E>(st + kGradBytes + 2 * kTile * 4 + e0 * 4, v);
+            }
+            // ranks c*8 .. c*8+rc-1 of this tile, in rank order
+            const int rc = P - c * kChunkRanks < kChunkRanks ? P - c * kChunkRanks : kChunkRanks;
+#pragma unroll
+            for (int q = 0; q < kChunkRanks; ++q)
+                if (q < rc) accumulate<E>(acc, smem_halves<E>(st + static_cast<size_t>(q) * kTile * 2 + e0 * 2));
+            if (c == nch - 1) {
+                float gm[E];
+                bool special = false;
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    gm[j] = finish_mean<PT>(acc[j], a);
+                    special |= !(isfinite(gm[j]) && isfinite(m[j]) && isfinite(v[j]));
+                }
+                // G = 2: the shortcuts for infinite operands are taken only by warps
+                // that hold a non-finite gradient mean or moment (one warp-uniform
+                // branch; both branches give the same IEEE results)
+                if (G == 1 || (G == 2 && __any_sync(__activemask(), special))) {
+#pragma unroll
+                    for (int j = 0; j < E; ++j) adam_elem<MODE, 1>(a, gm[j], w[j], m[j], v[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < E; ++j) adam_elem<MODE, 0>(a, gm[j], w[j], m[j], v[j]);
+                }
+                const long long i = i0 + e0;
+                store_floats<E>(w0 + i, w);
+                store_floats<E>(m0 + i, m);
+                store_floats<E>(v0 + i, v);
+                store_halves<E>(p0 + i, w); // all-gather: element head + i of the full vector
+            }
+        }
+    }
+
+    if (failed && tid == 0) {
+        // let the copies already issued land before the CTA's shared memory goes away
+        const long long issued_end = (u >= 1 ? u - 1 : 0) + kStages < units ? (u >= 1 ? u - 1 : 0) + kStages
+                                                                              : units;
+        for (long long k = u; k < issued_end; ++k)
+            (void)mbar_wait_bounded(&full[k % kStages], static_cast<uint32_t>((k / kStages) & 1));
+        atomicAdd(&g_wait_timeouts, 1u);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host side: validation, alignment analysis, launch
 // ---------------------------------------------------------------------------
 
@@ -317,6 +594,49 @@ KernelFn pick_kernel(int mode, int V, int P)
     }
 }
 
+// Consumer width of the bulk-copy kernel by P (measured on GB300): with few
+// ranks per tile the Adam arithmetic dominates and wants more warps; with
+// 8 ranks one 16-byte shared-memory read per rank per thread is best; with
+// more ranks the rank reduction wants more warps again.
+constexpr int tma_threads(int P)
+{
+    return P <= 4 ? 1024 : (P <= 8 ? 256 : 512);
+}
+
+struct TmaKernel {
+    KernelFn fn;
+    int threads;
+};
+
+template <int MODE, int PT>
+TmaKernel tma_instance()
+{
+    constexpr int NT = tma_threads(PT > 0 ? PT : 64);
+    return TmaKernel{zero_fused_step_tma_kernel<MODE, PT, NT, 2>, NT};
+}
+
+template <int MODE>
+TmaKernel pick_tma_p(int P)
+{
+    switch (P) {
+    case 4: return tma_instance<MODE, 4>();
+    case 8: return tma_instance<MODE, 8>();
+    case 16: return tma_instance<MODE, 16>();
+    case 32: return tma_instance<MODE, 32>();
+    case 64: return tma_instance<MODE, 64>();
+    default: return tma_instance<MODE, 0>();
+    }
+}
+
+TmaKernel pick_tma_kernel(int mode, int P)
+{
+    switch (mode) {
+    case ZERO_MODE_STANDARD: return pick_tma_p<ZERO_MODE_STANDARD>(P);
+    case ZERO_MODE_FOLDED_LITERAL: return pick_tma_p<ZERO_MODE_FOLDED_LITERAL>(P);
+    default: return pick_tma_p<ZERO_MODE_FOLDED_STORAGE>(P);
+    }
+}
+
 // Widest vector V in {8,4,2,1} for which one head length h makes every
 // stream's element h start on a V-element boundary (at most 16 bytes per
 // access, so fp32 streams need min(V,4)-element alignment).
@@ -361,6 +681,39 @@ int record_cuda(cudaError_t e)
     return ZERO_ECUDA;
 }
 
+// Launch set-up done once per (kernel, device): the resident CTAs per SM of
+// a vector-path kernel, or the dynamic shared-memory opt-in of a bulk-path
+// kernel.  Returns the value (>= 1) or ZERO_ECUDA.
+struct SetupEntry {
+    KernelFn fn;
+    int dev;
+    int value;
+};
+std::mutex g_setup_mu;
+SetupEntry g_setup[256];
+int g_setup_n = 0;
+
+int kernel_setup(KernelFn fn, bool bulk)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return record_cuda(e);
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    for (int i = 0; i < g_setup_n; ++i)
+        if (g_setup[i].fn == fn && g_setup[i].dev == dev) return g_setup[i].value;
+    int value = 1;
+    if (bulk) {
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kBulkSmem));
+    } else {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&value, fn, kThreads, 0);
+        if (value < 1) value = 1;
+    }
+    if (e != cudaSuccess) return record_cuda(e);
+    if (g_setup_n < 256) g_setup[g_setup_n++] = SetupEntry{fn, dev, value};
+    return value;
+}
+
 // Common validation of the hyper-parameters and sizes.
 int check_scalars(int64_t N, int32_t P, int32_t stage, int64_t t, float lr, float b1, float b2,
                   float eps, int32_t mode)
@@ -374,9 +727,9 @@ int check_scalars(int64_t N, int32_t P, int32_t stage, int64_t t, float lr, floa
     return ZERO_OK;
 }
 
-// Validate buffers and launch over the range described by `a` (n >= 1).
-int launch_range(StepArgs a, int64_t t, float lr, float b1, float b2, float eps, int mode,
-                 cudaStream_t stream)
+// Validate the buffers of the range described by `a` (n >= 1) and fill in
+// the step scalars; *V and the head are chosen from the buffers' alignment.
+int prepare_range(StepArgs& a, int64_t t, float lr, float b1, float b2, float eps, int* V)
 {
     if (!a.g || !a.w || !a.m || !a.v || !a.p) return ZERO_EINVAL;
     if (a.P > 1 && a.stride < a.n) return ZERO_EINVAL; // rank slices must not overlap
@@ -406,27 +759,61 @@ int launch_range(StepArgs a, int64_t t, float lr, float b1, float b2, float eps,
     a.bp2 = static_cast<float>(1.0 - std::pow(static_cast<double>(b2), static_cast<double>(t - 1)));
     a.p_pow2 = (a.P & (a.P - 1)) == 0;
     a.inv_p = 1.0f / static_cast<float>(a.P);
+    a.poison_tx = 0;
 
     long long head = 0;
-    const int V = pick_vector(a, &head);
+    *V = pick_vector(a, &head);
     a.head = head;
-    KernelFn fn = pick_kernel(mode, V, a.P);
+    return ZERO_OK;
+}
 
-    const int sms = sm_count_of_current_device();
-    if (sms <= 0) return record_cuda(cudaGetLastError());
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0);
-    if (e != cudaSuccess) return record_cuda(e);
-    if (per_sm < 1) per_sm = 1;
+// Tiles of the bulk range (elements [head, head + a multiple of 8)).
+long long bulk_tiles(const StepArgs& a)
+{
+    return ((a.n - a.head) / 8 * 8 + kTile - 1) / kTile;
+}
+
+int launch_tma(const StepArgs& a, int mode, int sms, cudaStream_t stream)
+{
+    const TmaKernel k = pick_tma_kernel(mode, a.P);
+    const int rc = kernel_setup(k.fn, true);
+    if (rc < 0) return rc;
+    k.fn<<<static_cast<unsigned int>(sms), k.threads, kBulkSmem, stream>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : record_cuda(e);
+}
+
+int launch_vector(const StepArgs& a, int V, int mode, int sms, cudaStream_t stream)
+{
+    KernelFn fn = pick_kernel(mode, V, a.P);
+    const int per_sm = kernel_setup(fn, false);
+    if (per_sm < 0) return per_sm;
     const long long body = (a.n - a.head) / V;
     long long blocks = (body + kThreads - 1) / kThreads;
     const long long cap = static_cast<long long>(sms) * per_sm;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     fn<<<static_cast<unsigned int>(blocks), kThreads, 0, stream>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return record_cuda(e);
-    return ZERO_OK;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : record_cuda(e);
+}
+
+// The bulk-copy pipeline needs every stream on one 16-byte phase (V = 8) and
+// pays off once every SM has a few tiles; smaller or misaligned problems take
+// the vector path, whose many CTAs start and finish sooner.
+constexpr int kMinTilesPerSm = 4;
+
+int launch_range(StepArgs a, int64_t t, float lr, float b1, float b2, float eps, int mode,
+                 cudaStream_t stream)
+{
+    int V = 1;
+    int rc = prepare_range(a, t, lr, b1, b2, eps, &V);
+    if (rc) return rc;
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return record_cuda(cudaGetLastError());
+    if (V == 8 && bulk_tiles(a) >= static_cast<long long>(kMinTilesPerSm) * sms)
+        return launch_tma(a, mode, sms, stream);
+    return launch_vector(a, V, mode, sms, stream);
 }
 
 } // namespace
@@ -480,6 +867,33 @@ extern "C" int zero_adam_step_shard(const void* grads_fp16, int64_t rank_stride,
     return launch_range(a, t, lr, beta1, beta2, eps, mode, static_cast<cudaStream_t>(cuda_stream));
 }
 
+extern "C" int zero_selftest_wait_timeout(const void* grads_fp16, int64_t rank_stride, float* master,
+                                          float* m, float* v, void* params_fp16, int64_t N, int32_t P,
+                                          int32_t stage, int64_t t, float lr, float beta1, float beta2,
+                                          float eps, int32_t mode, void* cuda_stream)
+{
+    int rc = check_scalars(N, P, stage, t, lr, beta1, beta2, eps, mode);
+    if (rc) return rc;
+    if (rank_stride < N) return ZERO_EINVAL;
+    StepArgs a{};
+    a.g = static_cast<const __half*>(grads_fp16);
+    a.stride = rank_stride;
+    a.w = master;
+    a.m = m;
+    a.v = v;
+    a.p = static_cast<__half*>(params_fp16);
+    a.n = N;
+    a.P = P;
+    int V = 1;
+    rc = prepare_range(a, t, lr, beta1, beta2, eps, &V);
+    if (rc) return rc;
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return record_cuda(cudaGetLastError());
+    if (V != 8 || bulk_tiles(a) < sms) return ZERO_EINVAL; // CTA 0 must own a bulk tile
+    a.poison_tx = 16; // 16 bytes that no copy will ever deliver
+    return launch_tma(a, mode, sms, static_cast<cudaStream_t>(cuda_stream));
+}
+
 extern "C" const char* zero_strerror(int code)
 {
     switch (code) {
@@ -491,6 +905,21 @@ extern "C" const char* zero_strerror(int code)
     case ZERO_ENOMEM: return "host allocation failed";
     default: return "unknown status code";
     }
+}
+
+extern "C" int zero_device_timeouts(int64_t* count, int32_t reset)
+{
+    if (!count) return ZERO_EINVAL;
+    unsigned int n = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&n, g_wait_timeouts, sizeof(n));
+    if (e != cudaSuccess) return record_cuda(e);
+    if (reset) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(zero));
+        if (e != cudaSuccess) return record_cuda(e);
+    }
+    *count = n;
+    return ZERO_OK;
 }
 
 extern "C" int zero_last_cuda_error(void) { return g_last_cuda_error; }
