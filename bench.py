@@ -57,6 +57,13 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="wall time budget of the CPU-oracle leg")
+    ap.add_argument("--overlap", action="store_true",
+                    help="time the bucketed step overlapped with a synthetic backward instead")
+    ap.add_argument("--bucket-elems", type=int, default=1 << 24)
+    ap.add_argument("--backward-k", type=int, default=2048,
+                    help="inner dimension of the synthetic backward's GEMMs")
+    ap.add_argument("--step-priority", choices=("high", "normal"), default="high",
+                    help="priority of the step's stream in the overlap leg")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -429,6 +436,128 @@ def run_e2e(z, wl, mode, g, master, m, v, params, stride, stream, device, dist, 
             "steps": K_e2e, "ms_per_step": ms / K_e2e}
 
 
+def run_overlap(args, wl, mode, dist):
+    """Bucketed step on a second stream behind a synthetic backward.
+
+    The backward pass is stood in for by one GEMM per bucket per rank,
+    dW = X_r @ Y (X_r: [L/768, k], Y: [k, 768], fp16 on the tensor cores),
+    written straight into rank r's gradient slice of the bucket, buckets in
+    backward order.  Reported: the backward alone, the whole step alone, the
+    two back to back on one stream, and the bucketed step on its own stream
+    waiting on one event per bucket; ``value`` is the fraction of the step's
+    time hidden behind the backward."""
+    import torch
+
+    import zero_sharded_mixed_shard_gb300 as z
+    from zero_sharded_mixed_shard_gb300 import synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the fused step has no CPU path)")
+    if wl.tensors is None or wl.shard is not None or any(n % 768 for n in wl.tensors):
+        raise SystemExit("--overlap needs a whole-vector workload with 768-multiple tensors (gpt2s)")
+    torch.cuda.set_device(dist.local_rank)
+    dist.init("nccl")
+    dev = torch.device("cuda", dist.local_rank)
+    P, N = wl.P, wl.N
+    stride = wl.rank_stride(True)
+    buckets = z.zero_plan_buckets(list(wl.tensors), args.bucket_elems, backward_order=True)
+    g = torch.zeros((P, stride), dtype=torch.float16, device=dev)
+    state = synth.torch_state(N, wl.seed, dev, wl.master_sigma)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.seed)
+    k = args.backward_k
+    rows_max = max((e - b) // 768 for b, e, _, _ in buckets)
+    X = [torch.randn(rows_max, k, generator=gen, device=dev).half() for _ in range(P)]
+    Y = (torch.randn(k, 768, generator=gen, device=dev) * (1e-3 / k ** 0.5)).half()
+    prod_stream = torch.cuda.Stream(dev)
+    # a higher-priority stream lets the step's CTAs take SMs as the backward's
+    # CTAs retire instead of queueing behind every later GEMM
+    step_stream = torch.cuda.Stream(dev, priority=-1 if args.step_priority == "high" else 0)
+    t_counter = [0]
+
+    def backward(stream, events=None):
+        with torch.cuda.stream(stream):
+            for i, (b, e, _, _) in enumerate(buckets):
+                rows = (e - b) // 768
+                for r in range(P):
+                    torch.mm(X[r][:rows], Y, out=g[r, b:e].view(rows, 768))
+                if events is not None:
+                    events[i].record(stream)
+
+    def step_whole(stream):
+        t_counter[0] += 1
+        z.zero_adam_step(g, stride, *state, N, P, wl.stage, t_counter[0], wl.lr, wl.b1, wl.b2,
+                         wl.eps, mode, stream)
+
+    def step_bucketed(stream, events):
+        t_counter[0] += 1
+        z.zero_adam_step_bucketed(g, stride, *state, N, P, wl.stage, t_counter[0], wl.lr, wl.b1,
+                                  wl.b2, wl.eps, mode, buckets, ready_events=events, stream=stream)
+
+    def timed(fn, reps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(step_stream)
+        for _ in range(reps):
+            fn()
+        done = torch.cuda.Event()
+        done.record(prod_stream)
+        step_stream.wait_event(done)
+        e1.record(step_stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def join(a, b):
+        ev = torch.cuda.Event()
+        ev.record(a)
+        b.wait_event(ev)
+
+    reps = max(3, min(args.steps, 50))
+
+    def only_backward():
+        join(step_stream, prod_stream)
+        backward(prod_stream)
+
+    def only_step():
+        join(prod_stream, step_stream)
+        step_whole(step_stream)
+
+    def serial():
+        join(step_stream, prod_stream)
+        backward(prod_stream)
+        step_whole(prod_stream)
+
+    def overlapped():
+        join(step_stream, prod_stream)
+        events = [torch.cuda.Event() for _ in buckets]
+        backward(prod_stream, events)
+        step_bucketed(step_stream, events)
+
+    t_b = timed(only_backward, reps)
+    t_s = timed(only_step, reps)
+    t_serial = timed(serial, reps)
+    t_over = timed(overlapped, reps)
+    hidden = (t_serial - t_over) / t_s
+    if dist.rank == 0:
+        line = {
+            "metric": "fraction of the optimizer step hidden behind a synthetic backward",
+            "value": hidden, "unit": "fraction", "n_gpus": dist.world, "steps": reps,
+            "warmup": args.warmup, "higher_is_better": True, "dtype": "f32",
+            "data": "synthetic", "config": dict(workload_config(wl, mode),
+                                                buckets=len(buckets), bucket_elems=args.bucket_elems,
+                                                backward="one fp16 GEMM [L/768,k]x[k,768] per bucket "
+                                                         f"per rank, k={k}",
+                                                step_stream_priority=args.step_priority),
+            "backward_ms": t_b, "step_ms": t_s, "serial_ms": t_serial, "overlapped_ms": t_over,
+            "gpu_launches_per_rep": len(buckets) * (P + 1),
+        }
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     from zero_sharded_mixed_shard_gb300 import synth
@@ -437,6 +566,8 @@ def main(argv=None):
     dist = Dist()
     if args.impl == "reference":
         return run_reference(args, wl, mode, dist)
+    if args.overlap:
+        return run_overlap(args, wl, mode, dist)
     return run_ours(args, wl, mode, dist)
 
 

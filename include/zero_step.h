@@ -196,6 +196,63 @@ int zero_adam_step_shard(const void* grads_fp16, int64_t rank_stride, int64_t gr
                          float lr, float beta1, float beta2, float eps, int32_t mode,
                          void* cuda_stream);
 
+/* ------------------------------------------------------------------------ */
+/* Buckets: the step of one part of the vector as soon as its gradients are  */
+/* ready ([P3] §1.5 通信数据量分析: gradients are bucketed so every 1/N is    */
+/* sent once, and sending overlaps the backward pass of earlier layers;       */
+/* [P3] §1.4: small tensors are bucketed and moved together; [P3] §1.6.7:    */
+/* separate CUDA streams let communication and computation run together).    */
+/* ------------------------------------------------------------------------ */
+
+/* One bucket: the flat range [begin, end) covering tensors first..last. */
+typedef struct {
+    int64_t begin;
+    int64_t end;
+    int32_t first_tensor;
+    int32_t last_tensor;
+} zero_bucket_t;
+
+/* Group consecutive tensors of the flat vector (tensor_numel[0..n_tensors))
+ * into buckets of at least bucket_elems elements each (the last bucket may be
+ * smaller); a tensor is never split, so a tensor larger than bucket_elems is a
+ * bucket of its own.  backward_order != 0 walks the tensors from the last to
+ * the first (the order a backward pass produces their gradients) and lists
+ * the buckets in that order; 0 walks them front to back.
+ * Two-call pattern: with buckets_out == NULL only *n_buckets is set;
+ * otherwise max_buckets is the capacity of buckets_out.  Host only.
+ * Errors: ZERO_EINVAL (null tensor_numel / n_buckets, n_tensors < 1, a
+ * negative size, total < 1, bucket_elems < 1, capacity too small). */
+int zero_plan_buckets(const int64_t* tensor_numel, int32_t n_tensors, int64_t bucket_elems,
+                      int32_t backward_order, zero_bucket_t* buckets_out, int32_t max_buckets,
+                      int32_t* n_buckets);
+
+/* The step of zero_adam_step restricted to flat elements [begin, end) of the
+ * whole-vector layout (all pointers are the full-vector bases; rank r's
+ * gradient of element i is at grads_fp16 + r * rank_stride + i).  The bytes
+ * written equal those zero_adam_step writes for these elements.
+ * Errors: as zero_adam_step, and ZERO_EINVAL unless 0 <= begin < end <= N. */
+int zero_adam_step_range(const void* grads_fp16, int64_t rank_stride, int64_t begin, int64_t end,
+                         float* master, float* m, float* v, void* params_fp16, int64_t N,
+                         int32_t P, int32_t stage, int64_t t, float lr, float beta1, float beta2,
+                         float eps, int32_t mode, void* cuda_stream);
+
+/* The whole step as n_buckets range steps enqueued on step_stream in list
+ * order; before bucket b the stream waits for ready_events[b] (a cudaEvent_t
+ * recorded by the producer of that bucket's gradients, e.g. on the stream of
+ * the backward pass; NULL = no wait).  The buckets must be disjoint
+ * sub-ranges of [0, N); together with any elements left out they give the
+ * same bytes as zero_adam_step.  The call only enqueues work: it returns
+ * before any bucket runs.
+ * Errors: as zero_adam_step; ZERO_EINVAL for a null bucket array, an empty
+ * or out-of-range bucket, or overlapping buckets (checked before anything is
+ * enqueued); ZERO_ECUDA if a wait or launch is refused (buckets enqueued
+ * before it stay enqueued). */
+int zero_adam_step_bucketed(const void* grads_fp16, int64_t rank_stride, float* master, float* m,
+                            float* v, void* params_fp16, int64_t N, int32_t P, int32_t stage,
+                            int64_t t, float lr, float beta1, float beta2, float eps, int32_t mode,
+                            const zero_bucket_t* buckets, int32_t n_buckets,
+                            void* const* ready_events, void* step_stream);
+
 /* Bounded waits that gave up, over every step launched on the current
  * device since the last reset.  The fused kernels wait on shared-memory
  * barriers for their own bulk copies; each wait gives up after 2 seconds,

@@ -118,3 +118,43 @@ def comm_elems_per_rank(N: int, stage: int) -> float:
     if stage == 3:
         return 3.0 * N
     raise ValueError("stage must be 0..3")
+
+
+def buckets(tensor_numel: list[int], bucket_elems: int, backward: bool = True
+            ) -> list[tuple[int, int, int, int]]:
+    """Group whole tensors into buckets of at least ``bucket_elems`` elements,
+    as (begin, end, first_tensor, last_tensor) of the flat vector.
+
+    Reading of 'bucket' (ZeRO 技术原理：进阶与 Offload §1.4 and §1.5: small
+    pieces are gathered into a bucket before they are sent; gradients are sent
+    bucket by bucket while the backward pass goes on): walk the tensors in the
+    order their gradients appear -- last to first for a backward pass -- and
+    close a bucket as soon as it holds bucket_elems elements; what is left at
+    the end is one more bucket, and trailing empty tensors join the previous
+    bucket."""
+    if bucket_elems < 1 or not tensor_numel or any(n < 0 for n in tensor_numel):
+        raise ValueError("bad bucket request")
+    starts = [0]
+    for n in tensor_numel:
+        starts.append(starts[-1] + n)
+    if starts[-1] < 1:
+        raise ValueError("empty vector")
+    order = list(range(len(tensor_numel)))
+    if backward:
+        order.reverse()
+    out, group, size = [], [], 0
+    for i in order:
+        group.append(i)
+        size += tensor_numel[i]
+        if size >= bucket_elems:
+            lo, hi = min(group), max(group)
+            out.append((starts[lo], starts[hi + 1], lo, hi))
+            group, size = [], 0
+    if group:
+        lo, hi = min(group), max(group)
+        if size > 0:
+            out.append((starts[lo], starts[hi + 1], lo, hi))
+        else:
+            b, e, plo, phi = out[-1]
+            out[-1] = (b, e, min(plo, lo), max(phi, hi))
+    return out

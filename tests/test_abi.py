@@ -109,3 +109,34 @@ def test_shard_rejects_and_empty_shard(zlib):
     assert shard(k=3, N=5, stride=2, g=None, w=None, m=None, v=None, p=None) == 0
     assert L.zero_adam_step_shard(None, 2, 0, 3, None, None, None, None, 5, 4, 2, 0, 1e-3, 0.9,
                                   0.999, 1e-8, 0, 0) == -1   # t = 0
+
+
+@no_gpu
+def test_range_and_bucketed_reject(zlib):
+    L = zlib.lib()
+
+    def rng_(b, e, N=1000):
+        return L.zero_adam_step_range(G, 1000, b, e, W, MM, V, PP, N, 4, 2, 1, 1e-3, 0.9, 0.999,
+                                      1e-8, 0, 0)
+
+    for b, e in [(-1, 10), (10, 10), (20, 10), (0, 1001)]:
+        assert rng_(b, e) == zlib.ZERO_EINVAL
+    assert rng_(0, 10, N=0) == zlib.ZERO_EINVAL
+
+    def bucketed(pairs, n=None):
+        arr = (zlib.zero_bucket_t * max(len(pairs), 1))()
+        for i, (b, e) in enumerate(pairs):
+            arr[i].begin, arr[i].end = b, e
+        return L.zero_adam_step_bucketed(G, 1000, W, MM, V, PP, 1000, 4, 2, 1, 1e-3, 0.9, 0.999,
+                                         1e-8, 0, arr, len(pairs) if n is None else n, None, 0)
+
+    assert bucketed([(0, 500), (400, 1000)]) == zlib.ZERO_EINVAL     # overlap
+    assert bucketed([(500, 1000), (0, 501)]) == zlib.ZERO_EINVAL     # overlap, unsorted
+    assert bucketed([(0, 500), (500, 1001)]) == zlib.ZERO_EINVAL     # past N
+    assert bucketed([(5, 5)]) == zlib.ZERO_EINVAL                    # empty
+    assert bucketed([(0, 10)], n=0) == zlib.ZERO_EINVAL
+    # valid buckets on a misaligned master pointer are refused before any launch
+    arr = (zlib.zero_bucket_t * 1)()
+    arr[0].begin, arr[0].end = 0, 1000
+    assert L.zero_adam_step_bucketed(G, 1000, W + 2, MM, V, PP, 1000, 4, 2, 1, 1e-3, 0.9, 0.999,
+                                     1e-8, 0, arr, 1, None, 0) == zlib.ZERO_EALIGN

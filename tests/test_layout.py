@@ -206,3 +206,62 @@ def test_lib_layout_rejects_bad_input(zlib):
         zlib.zero_shard_range(10, 4, 4)
     with pytest.raises(zlib.ZeroError):
         zlib.zero_memory_bytes(0, 4, 1)
+
+
+# ---------------------------------------------------------------------------
+# buckets
+# ---------------------------------------------------------------------------
+
+def test_bucket_invariants_brute_force():
+    rng = np.random.default_rng(4)
+    for _ in range(500):
+        numel = [int(x) for x in rng.integers(0, 12, size=int(rng.integers(1, 10)))]
+        if sum(numel) == 0:
+            numel[0] = 1
+        be = int(rng.integers(1, 30))
+        for backward in (True, False):
+            bs = L.buckets(numel, be, backward)
+            starts = np.concatenate([[0], np.cumsum(numel)])
+            # disjoint, non-empty, cover [0, N), in walk order
+            flat = sorted(bs)
+            assert flat[0][0] == 0 and flat[-1][1] == sum(numel)
+            for (b0, e0, *_), (b1, e1, *_) in zip(flat, flat[1:]):
+                assert e0 == b1
+            for k, (b, e, lo, hi) in enumerate(bs):
+                assert b < e
+                # whole tensors only
+                assert starts[lo] == b and starts[hi + 1] == e
+                # at least bucket_elems, except the last bucket in walk order
+                if k < len(bs) - 1:
+                    assert e - b >= be
+                    # minimal: dropping the last tensor added leaves it short
+                    last = lo if backward else hi
+                    assert (e - b) - numel[last] < be or numel[last] == 0
+            order = [b for b, *_ in bs]
+            assert order == sorted(order, reverse=backward)
+
+
+def test_lib_buckets_match_oracle(zlib):
+    from zero_sharded_mixed_shard_gb300 import synth
+    rng = np.random.default_rng(5)
+    cases = [([10, 5, 0, 3, 20, 1], 12), ([0, 0, 7, 0, 0], 3), ([1] * 50, 7), ([100], 1),
+             (synth.transformer_numels(), 1 << 25)]
+    for _ in range(300):
+        numel = [int(x) for x in rng.integers(0, 40, size=int(rng.integers(1, 15)))]
+        if sum(numel) == 0:
+            numel[-1] = 1
+        cases.append((numel, int(rng.integers(1, 100))))
+    for numel, be in cases:
+        for backward in (True, False):
+            assert zlib.zero_plan_buckets(numel, be, backward) == L.buckets(numel, be, backward)
+
+
+def test_lib_buckets_reject(zlib):
+    for numel, be in [([], 4), ([0, 0], 4), ([-1, 3], 4), ([5], 0)]:
+        with pytest.raises(zlib.ZeroError):
+            zlib.zero_plan_buckets(numel, be)
+    import ctypes
+    arr = (ctypes.c_int64 * 3)(5, 5, 5)
+    out = (zlib.zero_bucket_t * 1)()
+    n = ctypes.c_int32()
+    assert zlib.lib().zero_plan_buckets(arr, 3, 5, 1, out, 1, ctypes.byref(n)) == zlib.ZERO_EINVAL

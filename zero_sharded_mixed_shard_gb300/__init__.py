@@ -30,7 +30,8 @@ MODE_FOLDED_STORAGE = 2
 
 # every symbol include/zero_step.h declares
 EXPORTED = ("zero_init_layout", "zero_free_layout", "zero_shard_range", "zero_memory_bytes",
-            "zero_adam_step", "zero_adam_step_shard", "zero_device_timeouts",
+            "zero_adam_step", "zero_adam_step_shard", "zero_plan_buckets", "zero_adam_step_range",
+            "zero_adam_step_bucketed", "zero_device_timeouts",
             "zero_selftest_wait_timeout", "zero_strerror",
             "zero_last_cuda_error", "zero_last_cuda_error_string")
 
@@ -47,6 +48,11 @@ class ZeroError(RuntimeError):
 class zero_segment_t(ctypes.Structure):
     _fields_ = [("tensor_id", ctypes.c_int64), ("tensor_offset", ctypes.c_int64),
                 ("shard_offset", ctypes.c_int64), ("len", ctypes.c_int64)]
+
+
+class zero_bucket_t(ctypes.Structure):
+    _fields_ = [("begin", ctypes.c_int64), ("end", ctypes.c_int64),
+                ("first_tensor", ctypes.c_int32), ("last_tensor", ctypes.c_int32)]
 
 
 class zero_layout_t(ctypes.Structure):
@@ -94,6 +100,16 @@ def lib() -> ctypes.CDLL:
     L.zero_adam_step_shard.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp, i64, i32, i32, i64,
                                        f32, f32, f32, f32, i32, vp]
     L.zero_adam_step_shard.restype = ctypes.c_int
+    L.zero_plan_buckets.argtypes = [ctypes.POINTER(ctypes.c_int64), i32, i64, i32,
+                                    ctypes.POINTER(zero_bucket_t), i32, ctypes.POINTER(ctypes.c_int32)]
+    L.zero_plan_buckets.restype = ctypes.c_int
+    L.zero_adam_step_range.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i64, i32, i32, i64,
+                                       f32, f32, f32, f32, i32, vp]
+    L.zero_adam_step_range.restype = ctypes.c_int
+    L.zero_adam_step_bucketed.argtypes = [vp, i64, vp, vp, vp, vp, i64, i32, i32, i64,
+                                          f32, f32, f32, f32, i32, ctypes.POINTER(zero_bucket_t),
+                                          i32, ctypes.POINTER(ctypes.c_void_p), vp]
+    L.zero_adam_step_bucketed.restype = ctypes.c_int
     L.zero_selftest_wait_timeout.argtypes = [vp, i64, vp, vp, vp, vp, i64, i32, i32, i64,
                                              f32, f32, f32, f32, i32, vp]
     L.zero_selftest_wait_timeout.restype = ctypes.c_int
@@ -221,3 +237,55 @@ def zero_selftest_wait_timeout(grads, rank_stride: int, master, m, v, params, N:
                                           beta2, eps, mode, _stream(stream))
     if rc:
         raise ZeroError(rc, "zero_selftest_wait_timeout")
+
+
+def zero_plan_buckets(tensor_numel, bucket_elems: int, backward_order: bool = True) -> list:
+    """Buckets of consecutive tensors as (begin, end, first_tensor, last_tensor)."""
+    n = len(tensor_numel)
+    arr = (ctypes.c_int64 * max(n, 1))(*tensor_numel)
+    count = ctypes.c_int32()
+    rc = lib().zero_plan_buckets(arr, n, bucket_elems, 1 if backward_order else 0, None, 0,
+                                 ctypes.byref(count))
+    if rc:
+        raise ZeroError(rc, "zero_plan_buckets")
+    out = (zero_bucket_t * max(count.value, 1))()
+    rc = lib().zero_plan_buckets(arr, n, bucket_elems, 1 if backward_order else 0, out,
+                                 count.value, ctypes.byref(count))
+    if rc:
+        raise ZeroError(rc, "zero_plan_buckets")
+    return [(b.begin, b.end, b.first_tensor, b.last_tensor) for b in out[:count.value]]
+
+
+def zero_adam_step_range(grads, rank_stride: int, begin: int, end: int, master, m, v, params,
+                         N: int, P: int, stage: int, t: int, lr: float, beta1: float,
+                         beta2: float, eps: float, mode: int, stream=None) -> None:
+    """Enqueue the step of flat elements [begin, end) (see include/zero_step.h)."""
+    rc = lib().zero_adam_step_range(_addr(grads), rank_stride, begin, end, _addr(master),
+                                    _addr(m), _addr(v), _addr(params), N, P, stage, t, lr,
+                                    beta1, beta2, eps, mode, _stream(stream))
+    if rc:
+        raise ZeroError(rc, "zero_adam_step_range")
+
+
+def zero_adam_step_bucketed(grads, rank_stride: int, master, m, v, params, N: int, P: int,
+                            stage: int, t: int, lr: float, beta1: float, beta2: float,
+                            eps: float, mode: int, buckets, ready_events=None,
+                            stream=None) -> None:
+    """Enqueue the step bucket by bucket; bucket b waits for ready_events[b]
+    (torch.cuda.Event or None) on ``stream`` (see include/zero_step.h)."""
+    nb = len(buckets)
+    arr = (zero_bucket_t * max(nb, 1))()
+    for i, b in enumerate(buckets):
+        arr[i].begin, arr[i].end = int(b[0]), int(b[1])
+        arr[i].first_tensor = int(b[2]) if len(b) > 2 else -1
+        arr[i].last_tensor = int(b[3]) if len(b) > 3 else -1
+    evs = None
+    if ready_events is not None:
+        evs = (ctypes.c_void_p * max(nb, 1))()
+        for i, e in enumerate(ready_events):
+            evs[i] = None if e is None else (e if isinstance(e, int) else e.cuda_event)
+    rc = lib().zero_adam_step_bucketed(_addr(grads), rank_stride, _addr(master), _addr(m),
+                                       _addr(v), _addr(params), N, P, stage, t, lr, beta1,
+                                       beta2, eps, mode, arr, nb, evs, _stream(stream))
+    if rc:
+        raise ZeroError(rc, "zero_adam_step_bucketed")

@@ -145,3 +145,59 @@ extern "C" int zero_init_layout(const int64_t* tensor_numel, int32_t n_tensors, 
     *out = t;
     return ZERO_OK;
 }
+
+// Buckets of consecutive tensors, each at least bucket_elems long (the last
+// one may be shorter); tensors are never split.  In backward order the walk
+// starts from the last tensor, the order in which a backward pass finishes
+// the gradients ([P3] §1.5: bucketed gradients, sent while earlier layers'
+// gradients are still being computed).
+extern "C" int zero_plan_buckets(const int64_t* tensor_numel, int32_t n_tensors, int64_t bucket_elems,
+                                 int32_t backward_order, zero_bucket_t* buckets_out, int32_t max_buckets,
+                                 int32_t* n_buckets)
+{
+    if (!tensor_numel || !n_buckets || n_tensors < 1 || bucket_elems < 1) return ZERO_EINVAL;
+    std::vector<int64_t> start(static_cast<size_t>(n_tensors) + 1, 0);
+    for (int32_t i = 0; i < n_tensors; ++i) {
+        if (tensor_numel[i] < 0 || tensor_numel[i] > INT64_MAX - start[i]) return ZERO_EINVAL;
+        start[i + 1] = start[i] + tensor_numel[i];
+    }
+    if (start[n_tensors] < 1) return ZERO_EINVAL;
+
+    int32_t count = 0;
+    int64_t acc = 0;
+    int32_t first = -1; // tensor that opened the current bucket (in walk order)
+    auto emit = [&](int32_t lo, int32_t hi) -> bool {
+        // tensors lo..hi in flat order
+        if (buckets_out) {
+            if (count >= max_buckets) return false;
+            buckets_out[count] = zero_bucket_t{start[lo], start[hi + 1], lo, hi};
+        }
+        ++count;
+        return true;
+    };
+    for (int32_t step = 0; step < n_tensors; ++step) {
+        const int32_t i = backward_order ? n_tensors - 1 - step : step;
+        if (first < 0) first = i;
+        acc += tensor_numel[i];
+        if (acc >= bucket_elems) {
+            const int32_t lo = first < i ? first : i, hi = first < i ? i : first;
+            if (!emit(lo, hi)) return ZERO_EINVAL;
+            first = -1;
+            acc = 0;
+        }
+    }
+    if (first >= 0) {
+        const int32_t last = backward_order ? 0 : n_tensors - 1;
+        const int32_t lo = first < last ? first : last, hi = first < last ? last : first;
+        if (acc > 0 || count == 0) {
+            if (!emit(lo, hi)) return ZERO_EINVAL;
+        } else if (count > 0 && buckets_out) {
+            // only empty tensors are left: fold them into the previous bucket
+            zero_bucket_t& b = buckets_out[count - 1];
+            if (lo < b.first_tensor) b.first_tensor = lo;
+            if (hi > b.last_tensor) b.last_tensor = hi;
+        }
+    }
+    *n_buckets = count;
+    return ZERO_OK;
+}

@@ -24,10 +24,13 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "zero_step.h"
 
@@ -865,6 +868,79 @@ extern "C" int zero_adam_step_shard(const void* grads_fp16, int64_t rank_stride,
     a.n = len;
     a.P = P;
     return launch_range(a, t, lr, beta1, beta2, eps, mode, static_cast<cudaStream_t>(cuda_stream));
+}
+
+namespace {
+
+// The range [begin, end) of the whole-vector layout as a StepArgs.
+StepArgs range_args(const void* grads_fp16, int64_t rank_stride, int64_t begin, int64_t end, float* master,
+                    float* m, float* v, void* params_fp16, int32_t P)
+{
+    StepArgs a{};
+    a.g = static_cast<const __half*>(grads_fp16) + begin;
+    a.stride = rank_stride;
+    a.w = master + begin;
+    a.m = m + begin;
+    a.v = v + begin;
+    a.p = static_cast<__half*>(params_fp16) + begin;
+    a.n = end - begin;
+    a.P = P;
+    return a;
+}
+
+} // namespace
+
+extern "C" int zero_adam_step_range(const void* grads_fp16, int64_t rank_stride, int64_t begin, int64_t end,
+                                    float* master, float* m, float* v, void* params_fp16, int64_t N,
+                                    int32_t P, int32_t stage, int64_t t, float lr, float beta1, float beta2,
+                                    float eps, int32_t mode, void* cuda_stream)
+{
+    int rc = check_scalars(N, P, stage, t, lr, beta1, beta2, eps, mode);
+    if (rc) return rc;
+    if (rank_stride < N || begin < 0 || begin >= end || end > N) return ZERO_EINVAL;
+    if (!grads_fp16 || !master || !m || !v || !params_fp16) return ZERO_EINVAL;
+    return launch_range(range_args(grads_fp16, rank_stride, begin, end, master, m, v, params_fp16, P), t, lr,
+                        beta1, beta2, eps, mode, static_cast<cudaStream_t>(cuda_stream));
+}
+
+extern "C" int zero_adam_step_bucketed(const void* grads_fp16, int64_t rank_stride, float* master, float* m,
+                                       float* v, void* params_fp16, int64_t N, int32_t P, int32_t stage,
+                                       int64_t t, float lr, float beta1, float beta2, float eps, int32_t mode,
+                                       const zero_bucket_t* buckets, int32_t n_buckets,
+                                       void* const* ready_events, void* step_stream)
+{
+    int rc = check_scalars(N, P, stage, t, lr, beta1, beta2, eps, mode);
+    if (rc) return rc;
+    if (rank_stride < N || !buckets || n_buckets < 1) return ZERO_EINVAL;
+    if (!grads_fp16 || !master || !m || !v || !params_fp16) return ZERO_EINVAL;
+    // every bucket in range and no two overlapping, before anything is enqueued
+    std::vector<std::pair<int64_t, int64_t>> sorted;
+    sorted.reserve(static_cast<size_t>(n_buckets));
+    for (int32_t b = 0; b < n_buckets; ++b) {
+        if (buckets[b].begin < 0 || buckets[b].begin >= buckets[b].end || buckets[b].end > N) return ZERO_EINVAL;
+        sorted.emplace_back(buckets[b].begin, buckets[b].end);
+    }
+    std::sort(sorted.begin(), sorted.end());
+    for (size_t i = 1; i < sorted.size(); ++i)
+        if (sorted[i].first < sorted[i - 1].second) return ZERO_EINVAL;
+    // the buffers are validated once, for the whole vector
+    StepArgs whole = range_args(grads_fp16, rank_stride, 0, N, master, m, v, params_fp16, P);
+    int V = 1;
+    rc = prepare_range(whole, t, lr, beta1, beta2, eps, &V);
+    if (rc) return rc;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(step_stream);
+    for (int32_t b = 0; b < n_buckets; ++b) {
+        if (ready_events && ready_events[b]) {
+            const cudaError_t e = cudaStreamWaitEvent(stream, static_cast<cudaEvent_t>(ready_events[b]), 0);
+            if (e != cudaSuccess) return record_cuda(e);
+        }
+        rc = launch_range(range_args(grads_fp16, rank_stride, buckets[b].begin, buckets[b].end, master, m, v,
+                                     params_fp16, P),
+                          t, lr, beta1, beta2, eps, mode, stream);
+        if (rc) return rc;
+    }
+    return ZERO_OK;
 }
 
 extern "C" int zero_selftest_wait_timeout(const void* grads_fp16, int64_t rank_stride, float* master,

@@ -9,7 +9,7 @@ parameter vector of N elements, P data-parallel ranks each holding an fp16
 local gradient of the whole vector, fp32 master / momentum / variance):
 
 * ``tiny``     N = 1,000,003 (P does not divide N), P = 4, ZeRO-2
-* ``gpt2s``    N = 124,439,808 (GPT-2-small sized flat vector), P = 8, ZeRO-1,
+* ``gpt2s``    N = 124,439,808 (GPT-2 small's tensors, flattened), P = 8, ZeRO-1,
                1 % of gradient entries scaled x100 (heavy tail)
 * ``tf1p3b``   N = 1.3e9 as 24 transformer layers at d = 2048 plus one
                embedding tensor, P = 16, ZeRO-2 (shard cuts cross tensors)
@@ -49,6 +49,15 @@ def transformer_numels(layers: int = 24, d: int = 2048, total: int = 1_300_000_0
     if rest < 0:
         raise ValueError("the blocks alone exceed the requested total")
     return body + ([rest] if rest else [])
+
+
+def gpt2_small_numels(d: int = 768, layers: int = 12, vocab: int = 50257, ctx: int = 1024) -> list[int]:
+    """GPT-2 small's tensors in flat order: token and position embeddings,
+    12 blocks (LayerNorm 1, fused QKV weight and bias, attention projection,
+    LayerNorm 2, MLP up and down projections) and the final LayerNorm:
+    124,439,808 parameters, every size a multiple of 768."""
+    block = [d, d, d * 3 * d, 3 * d, d * d, d, d, d, d * 4 * d, 4 * d, 4 * d * d, d]
+    return [vocab * d, ctx * d] + block * layers + [d, d]
 
 
 def round_up(x: int, q: int) -> int:
@@ -107,7 +116,8 @@ WORKLOADS = {
     "tiny": Workload("tiny", N=1_000_003, P=4, stage=2, modes=(0,), steps=10,
                      grad_sigma=1e-3, seed=1000),
     "gpt2s": Workload("gpt2s", N=124_439_808, P=8, stage=1, modes=(0,), steps=20,
-                      grad_sigma=1e-3, heavy_tail_frac=0.01, seed=1001),
+                      grad_sigma=1e-3, heavy_tail_frac=0.01, seed=1001,
+                      tensors=tuple(gpt2_small_numels())),
     "tf1p3b": Workload("tf1p3b", N=1_300_000_000, P=16, stage=2, modes=(0,), steps=5,
                        grad_sigma=1e-4, tensors=tuple(transformer_numels()), seed=1002),
     "shard7p5b": Workload("shard7p5b", N=7_500_000_000, P=64, stage=3, modes=(0,), steps=5,
