@@ -70,6 +70,9 @@ def _load():
     lib.oracle_zero_step.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp, i64,
                                      f32, f32, f32, f32, i32, i32]
     lib.oracle_zero_step.restype = ctypes.c_int
+    lib.oracle_offload_elems.argtypes = [vp, i64, i32, vp, vp, vp, vp, vp, i64, i64,
+                                         f32, f32, f32, f32, i32]
+    lib.oracle_offload_elems.restype = ctypes.c_int
     lib.oracle_adam_elems_f64.argtypes = [vp, i64, i32, vp, vp, vp, i64, i64,
                                           f64, f64, f64, f64, i32]
     lib.oracle_adam_elems_f64.restype = ctypes.c_int
@@ -159,3 +162,22 @@ def adam_elems_f64(grads, rank_stride: int, P: int, w: np.ndarray, m: np.ndarray
     rc = _load().oracle_adam_elems_f64(_ptr(g), rank_stride, P, _ptr(w), _ptr(m),
                                        _ptr(v), n, t, lr, b1, b2, eps, mode)
     _check(rc, "adam_elems_f64")
+
+
+def offload_elems(grads, rank_stride: int, P: int, master: np.ndarray, m: np.ndarray,
+                  v: np.ndarray, t: int, lr: float, b1: float, b2: float, eps: float,
+                  mode: int) -> tuple[np.ndarray, np.ndarray]:
+    """ZeRO-Offload's elementwise step (gradient mean crosses to the CPU as
+    fp16), in place on master / m / v.  Returns (fp16 codes of the new
+    weights, fp16 codes of the gradient that crossed)."""
+    g = _as_u16(grads).reshape(-1)
+    n = master.size
+    for a in (master, m, v):
+        assert a.dtype == np.float32 and a.size == n and a.flags["C_CONTIGUOUS"]
+    assert P >= 1 and (n == 0 or g.size >= (P - 1) * rank_stride + n)
+    out = np.empty(n, np.uint16)
+    g16 = np.empty(n, np.uint16)
+    rc = _load().oracle_offload_elems(_ptr(g), rank_stride, P, _ptr(master), _ptr(m), _ptr(v),
+                                      _ptr(out), _ptr(g16), n, t, lr, b1, b2, eps, mode)
+    _check(rc, "offload_elems")
+    return out, g16

@@ -356,6 +356,38 @@ int oracle_zero_step(const uint16_t* grads, int64_t rank_stride, int32_t P, int6
     return rc;
 }
 
+/* ZeRO-Offload's update ([P3] ZeRO 技术原理：进阶与 Offload §2.2 Offload 策略:
+ * the data-flow graph is cut along the fp16 gradient and fp16 parameter
+ * edges, so the optimizer update and the float2half node run on the CPU;
+ * §2.3: each GPU hands its 1/N shard of fp16 gradients to a CPU process).
+ * The gradient mean is formed as in reduce_mean, then crosses to the CPU as
+ * fp16 (rounded to nearest even) and is widened back before Adam; the rest
+ * is the same update and cast.  g16_out (optional, n codes) receives the
+ * fp16 gradient that crossed. */
+int oracle_offload_elems(const uint16_t* grads, int64_t rank_stride, int32_t P,
+                         float* w, float* m, float* v, uint16_t* params_out, uint16_t* g16_out,
+                         int64_t n, int64_t t, float lr, float b1, float b2, float eps,
+                         int32_t mode)
+{
+    int rc = check_common(P, t, mode);
+    if (rc) return rc;
+    if (n < 0) return -2;
+    if (n == 0) return 0;
+    const step_scalars s = make_scalars(t, lr, b1, b2, eps, mode);
+    float* g = (float*)malloc((size_t)n * sizeof(float));
+    if (!g) return -1;
+    reduce_mean(grads, rank_stride, P, n, g);                 /* on the GPU */
+    for (int64_t j = 0; j < n; ++j) {                          /* the fp16 gradient edge */
+        const uint16_t h = oracle_float_to_half(g[j]);
+        if (g16_out) g16_out[j] = h;
+        g[j] = oracle_half_to_float(h);
+    }
+    adam_update(&s, g, w, m, v, n);                            /* on the CPU */
+    cast_half(w, params_out, n);                               /* float2half on the CPU */
+    free(g);
+    return 0;
+}
+
 /* Double-precision evaluation of the same formulas, for error-bound checks of
  * the fp32 path on small inputs (not a parity reference: the fp32 oracle is).
  * State in double, gradients given as fp16 codes, output weights in double. */

@@ -248,3 +248,52 @@ def test_folded_storage_tracks_standard(oracle_mod):
     assert np.max(np.abs(s2[0].astype(np.float64) - s0[0])) <= T * 1e-3 * 1e-5
     bc1 = 1 - f64(B1) ** T
     assert np.allclose(s2[1], s0[1] / bc1, rtol=1e-3, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# ZeRO-Offload (ZeRO 技术原理：进阶与 Offload §2.2: the fp16 gradient crosses to
+# the CPU, which runs the update and float2half)
+# ---------------------------------------------------------------------------
+
+def _rank_order_mean_fp16(codes, stride, P, n):
+    """numpy: fp32 sum in rank order (one rounded add per rank), / P, to fp16."""
+    x = codes.view(np.float16).reshape(P, stride)[:, :n].astype(np.float32)
+    acc = np.zeros(n, np.float32)
+    for r in range(P):
+        acc = acc + x[r]
+    return (acc / np.float32(P)).astype(np.float16)
+
+
+@pytest.mark.parametrize("P", [1, 3, 4, 8, 16])
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_offload_is_the_step_on_the_fp16_mean(oracle_mod, P, mode):
+    from zero_sharded_mixed_shard_gb300 import synth
+    n, stride = 5000, 5003
+    codes = synth.np_grads(P, n, stride, 1e-3, 60 + P, heavy_tail_frac=0.05)
+    w0, m0, v0, _ = synth.np_state(n, 61)
+    a = [w0.copy(), m0.copy(), v0.copy()]
+    p_off, g16 = oracle_mod.offload_elems(codes, stride, P, *a, 2, 1e-3, 0.9, 0.999, 1e-8, mode)
+    # the gradient that crossed is numpy's fp16 of the rank-order mean
+    mean16 = _rank_order_mean_fp16(codes, stride, P, n)
+    assert np.array_equal(g16, mean16.view(np.uint16))
+    # and the rest is exactly the one-rank step on that gradient
+    b = [w0.copy(), m0.copy(), v0.copy()]
+    p_one = oracle_mod.adam_elems(mean16.view(np.uint16), n, 1, *b, 2, 1e-3, 0.9, 0.999, 1e-8,
+                                  mode)
+    assert np.array_equal(p_off, p_one)
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+
+
+def test_offload_differs_from_fused_only_through_the_gradient_rounding(oracle_mod):
+    # with gradients whose mean is exactly an fp16 value the two agree bit for bit
+    n, P = 64, 4
+    j = np.arange(n)
+    ranks = np.array([(r + 1 + j) * 2.0 ** -12 for r in range(P)], np.float16)
+    codes = ranks.view(np.uint16).reshape(-1)
+    w0 = np.linspace(-1, 1, n).astype(np.float32)
+    a = [w0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    b = [w0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    p1, _ = oracle_mod.offload_elems(codes, n, P, *a, 1, 1e-3, 0.9, 0.999, 1e-8, 0)
+    p2 = oracle_mod.adam_elems(codes, n, P, *b, 1, 1e-3, 0.9, 0.999, 1e-8, 0)
+    assert np.array_equal(p1, p2)

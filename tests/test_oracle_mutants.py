@@ -34,6 +34,7 @@ MUTANTS = {
     "half exponent bias": ("ldexpf((float)(1024 + frac), expo - 25)",
                            "ldexpf((float)(1024 + frac), expo - 24)"),
     "all-gather offset": ("memcpy(params + begin, shard_half", "memcpy(params + begin / 2, shard_half"),
+    "offload gradient not rounded": ("g[j] = oracle_half_to_float(h);", "(void)h;"),
     "last shard loses its clamped tail": ("const int64_t end = begin + M < N ? begin + M : N;",
                                           "const int64_t end = begin + M < N ? begin + M : N - 1;"),
 }
