@@ -64,6 +64,8 @@ def parse_args(argv=None):
                     help="inner dimension of the synthetic backward's GEMMs")
     ap.add_argument("--step-priority", choices=("high", "normal"), default="high",
                     help="priority of the step's stream in the overlap leg")
+    ap.add_argument("--offload", action="store_true",
+                    help="time the ZeRO-Offload step (update on the host CPU) instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -558,6 +560,87 @@ def run_overlap(args, wl, mode, dist):
     return 0
 
 
+def run_offload(args, wl, mode, dist):
+    """ZeRO-Offload step: fp16 gradient mean to page-locked host memory, CPU
+    Adam per shard in stream order, fp16 weights back into the device
+    vector.  Also timed alone: the GPU reduce (its host writes) and the host
+    Adam on all host cores."""
+    import torch
+
+    import zero_sharded_mixed_shard_gb300 as z
+    from zero_sharded_mixed_shard_gb300 import synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the fused step has no CPU path)")
+    if wl.shard is not None:
+        raise SystemExit("--offload runs whole-vector workloads")
+    torch.cuda.set_device(dist.local_rank)
+    dist.init("nccl")
+    dev = torch.device("cuda", dist.local_rank)
+    P, N = wl.P, wl.N
+    stride = wl.rank_stride(True)
+    cores = os.cpu_count() or 1
+    g = synth.torch_grads(P, N, stride, wl.grad_sigma, wl.seed, dev, wl.heavy_tail_frac,
+                          wl.zero_frac, step=1)
+    dstate = synth.torch_state(N, wl.seed, dev, wl.master_sigma)
+    host = [torch.empty(N, dtype=torch.float32, pin_memory=True) for _ in range(3)]
+    for h, d in zip(host, dstate[:3]):
+        h.copy_(d)
+    g16_h = torch.empty(N, dtype=torch.float16, pin_memory=True)
+    p16_h = torch.empty(N, dtype=torch.float16, pin_memory=True)
+    params = dstate[3]
+    stream = torch.cuda.current_stream(dev)
+    t = [0]
+
+    def step():
+        t[0] += 1
+        z.zero_offload_step(g, stride, *host, g16_h, p16_h, params, N, P, wl.stage, t[0], wl.lr,
+                            wl.b1, wl.b2, wl.eps, mode, cores, stream)
+
+    def reduce_only():
+        z.zero_reduce_scatter_fp16(g, stride, 0, P, N, g16_h, stream)
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return dist.max(e0.elapsed_time(e1) / reps, dev)
+
+    reps = max(3, min(args.steps, 20))
+    ms_step = timed(step, reps)
+    ms_reduce = timed(reduce_only, reps)
+    # the host update alone, all cores, same buffers
+    t0 = time.perf_counter()
+    for k in range(reps):
+        z.zero_cpu_adam(g16_h, *host, p16_h, N, t[0] + k + 1, wl.lr, wl.b1, wl.b2, wl.eps, mode,
+                        cores)
+    ms_cpu = (time.perf_counter() - t0) * 1e3 / reps
+    if dist.rank == 0:
+        line = {
+            "metric": "params updated/sec, ZeRO-Offload step (update on the host CPU)",
+            "value": N * dist.world / (ms_step / 1e3), "unit": "params/s", "n_gpus": dist.world,
+            "steps": reps, "warmup": 3, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "dtype": "f32", "data": "synthetic (seeded device RNG)",
+            "config": dict(workload_config(wl, mode), state="fp32 master/m/v in page-locked host memory"),
+            "reduce_ms": ms_reduce,
+            "reduce_gbs": (2 * P + 2) * N / (ms_reduce / 1e3) / 1e9,
+            "cpu_adam_ms": ms_cpu, "cpu_adam_params_per_s": N / (ms_cpu / 1e3), "cpu_cores": cores,
+            "cpu_adam_host_gbs": 28 * N / (ms_cpu / 1e3) / 1e9,
+            "host_link_bytes_per_step": {"d2h_fp16_gradient": 2 * N, "h2d_fp16_params": 2 * N},
+            "device_state_bytes_saved": 12 * N,
+        }
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     from zero_sharded_mixed_shard_gb300 import synth
@@ -568,6 +651,8 @@ def main(argv=None):
         return run_reference(args, wl, mode, dist)
     if args.overlap:
         return run_overlap(args, wl, mode, dist)
+    if args.offload:
+        return run_offload(args, wl, mode, dist)
     return run_ours(args, wl, mode, dist)
 
 

@@ -253,6 +253,62 @@ int zero_adam_step_bucketed(const void* grads_fp16, int64_t rank_stride, float* 
                             const zero_bucket_t* buckets, int32_t n_buckets,
                             void* const* ready_events, void* step_stream);
 
+/* ------------------------------------------------------------------------ */
+/* ZeRO-Offload ([P3] §2.2 Offload 策略: the data-flow graph is cut along    */
+/* the fp16 gradient and fp16 parameter edges, so the parameter update and   */
+/* float2half run on the CPU beside the Adam state in host memory; §2.3: each */
+/* GPU's 1/N shard is updated by a CPU process; §1.6.6: that CPU Adam uses    */
+/* multithreading and SIMD).  These are explicit entry points of their own: */
+/* the fused GPU step never falls back to them.                              */
+/* ------------------------------------------------------------------------ */
+
+/* GPU side of the offloaded step: out_fp16[i] = fp16_rne((sum over ranks
+ * r = 0..P-1, in order, of grads_fp16[grad_offset + r * rank_stride + i]) / P)
+ * for i in [0, n), the mean formed exactly as zero_adam_step forms it.
+ * out_fp16 may be device memory or page-locked host memory (the kernel then
+ * writes across the host link itself).  Enqueued on cuda_stream.
+ * Errors: ZERO_EINVAL (null pointer, n < 1, P outside [1, ZERO_MAX_RANKS],
+ * grad_offset < 0, rank_stride < n when P > 1), ZERO_EALIGN (a pointer not
+ * 2-byte aligned), ZERO_EOVERLAP (out_fp16 inside the gradients),
+ * ZERO_ECUDA. */
+int zero_reduce_scatter_fp16(const void* grads_fp16, int64_t rank_stride, int64_t grad_offset,
+                             int32_t P, int64_t n, void* out_fp16, void* cuda_stream);
+
+/* CPU side of the offloaded step, on host memory: Adam on n elements of
+ * fp32 master / m / v from the fp16 gradient grad_fp16, and the fp16 cast of
+ * the new weights into params_fp16 -- the same operations, in the same order
+ * and precision, as zero_adam_step (given the gradient).  `threads` host
+ * threads take chunks of 16 Ki elements as they are free (0 = one per
+ * hardware thread; the calling thread is one of them).  Runs synchronously
+ * on the calling thread.
+ * Errors: ZERO_EINVAL (null pointer with n > 0, n < 0, t < 1, bad mode or
+ * hyper-parameter, threads outside [0, 1024]). */
+int zero_cpu_adam(const void* grad_fp16, float* master, float* m, float* v, void* params_fp16,
+                  int64_t n, int64_t t, float lr, float beta1, float beta2, float eps,
+                  int32_t mode, int32_t threads);
+
+/* One ZeRO-Offload step of the whole vector, enqueued on cuda_stream:
+ *   1. zero_reduce_scatter_fp16 of all N elements into grad16_host;
+ *   2. one host function (cudaLaunchHostFunc) that runs zero_cpu_adam over
+ *      every shard k = 0..P-1 ([min(kM,N), min((k+1)M,N)), contiguous, so
+ *      one pass over [0, N)) with cpu_threads host threads (0 = all
+ *      hardware threads) taking chunks as they are free, writing
+ *      params16_host;
+ *   3. one async copy per shard of its fp16 weights into params_fp16 at
+ *      offset kM (the all-gather's output).
+ * grads_fp16 and params_fp16 are device memory; master_host, m_host, v_host
+ * (fp32 [N]) and grad16_host, params16_host (fp16 [N]) are page-locked host
+ * memory that the caller keeps alive, and leaves alone, until the stream has
+ * passed this step.  The call returns at once.  Numerically the step differs
+ * from zero_adam_step only in that the gradient mean is rounded to fp16 on
+ * its way to the host.  Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ENOMEM (host
+ * bookkeeping), ZERO_ECUDA (work enqueued before the refused call stays
+ * enqueued). */
+int zero_offload_step(const void* grads_fp16, int64_t rank_stride, float* master_host, float* m_host,
+                      float* v_host, void* grad16_host, void* params16_host, void* params_fp16,
+                      int64_t N, int32_t P, int32_t stage, int64_t t, float lr, float beta1,
+                      float beta2, float eps, int32_t mode, int32_t cpu_threads, void* cuda_stream);
+
 /* Bounded waits that gave up, over every step launched on the current
  * device since the last reset.  The fused kernels wait on shared-memory
  * barriers for their own bulk copies; each wait gives up after 2 seconds,

@@ -31,7 +31,8 @@ MODE_FOLDED_STORAGE = 2
 # every symbol include/zero_step.h declares
 EXPORTED = ("zero_init_layout", "zero_free_layout", "zero_shard_range", "zero_memory_bytes",
             "zero_adam_step", "zero_adam_step_shard", "zero_plan_buckets", "zero_adam_step_range",
-            "zero_adam_step_bucketed", "zero_device_timeouts",
+            "zero_adam_step_bucketed", "zero_reduce_scatter_fp16", "zero_cpu_adam",
+            "zero_offload_step", "zero_device_timeouts",
             "zero_selftest_wait_timeout", "zero_strerror",
             "zero_last_cuda_error", "zero_last_cuda_error_string")
 
@@ -110,6 +111,13 @@ def lib() -> ctypes.CDLL:
                                           f32, f32, f32, f32, i32, ctypes.POINTER(zero_bucket_t),
                                           i32, ctypes.POINTER(ctypes.c_void_p), vp]
     L.zero_adam_step_bucketed.restype = ctypes.c_int
+    L.zero_reduce_scatter_fp16.argtypes = [vp, i64, i64, i32, i64, vp, vp]
+    L.zero_reduce_scatter_fp16.restype = ctypes.c_int
+    L.zero_cpu_adam.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, f32, f32, f32, i32, i32]
+    L.zero_cpu_adam.restype = ctypes.c_int
+    L.zero_offload_step.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, i64, i32, i32, i64,
+                                    f32, f32, f32, f32, i32, i32, vp]
+    L.zero_offload_step.restype = ctypes.c_int
     L.zero_selftest_wait_timeout.argtypes = [vp, i64, vp, vp, vp, vp, i64, i32, i32, i64,
                                              f32, f32, f32, f32, i32, vp]
     L.zero_selftest_wait_timeout.restype = ctypes.c_int
@@ -134,10 +142,12 @@ def zero_strerror(code: int) -> str:
 
 
 def _addr(x) -> int | None:
-    """Device address of a tensor (or pass an int / None through)."""
+    """Address of a torch tensor or numpy array (or pass an int / None through)."""
     if x is None or isinstance(x, int):
         return x
-    return x.data_ptr()
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return x.__array_interface__["data"][0]
 
 
 def _stream(stream) -> int | None:
@@ -289,3 +299,36 @@ def zero_adam_step_bucketed(grads, rank_stride: int, master, m, v, params, N: in
                                        beta2, eps, mode, arr, nb, evs, _stream(stream))
     if rc:
         raise ZeroError(rc, "zero_adam_step_bucketed")
+
+
+def zero_reduce_scatter_fp16(grads, rank_stride: int, grad_offset: int, P: int, n: int, out,
+                             stream=None) -> None:
+    """Enqueue the fp16 gradient mean of n elements into ``out`` (device or
+    page-locked host memory; see include/zero_step.h)."""
+    rc = lib().zero_reduce_scatter_fp16(_addr(grads), rank_stride, grad_offset, P, n, _addr(out),
+                                        _stream(stream))
+    if rc:
+        raise ZeroError(rc, "zero_reduce_scatter_fp16")
+
+
+def zero_cpu_adam(grad16, master, m, v, params16, n: int, t: int, lr: float, beta1: float,
+                  beta2: float, eps: float, mode: int, threads: int = 0) -> None:
+    """ZeRO-Offload's host update on host buffers (numpy arrays, page-locked
+    torch tensors or addresses); runs synchronously."""
+    rc = lib().zero_cpu_adam(_addr(grad16), _addr(master), _addr(m), _addr(v), _addr(params16), n,
+                             t, lr, beta1, beta2, eps, mode, threads)
+    if rc:
+        raise ZeroError(rc, "zero_cpu_adam")
+
+
+def zero_offload_step(grads, rank_stride: int, master_host, m_host, v_host, grad16_host,
+                      params16_host, params, N: int, P: int, stage: int, t: int, lr: float,
+                      beta1: float, beta2: float, eps: float, mode: int, cpu_threads: int = 0,
+                      stream=None) -> None:
+    """Enqueue one ZeRO-Offload step (see include/zero_step.h)."""
+    rc = lib().zero_offload_step(_addr(grads), rank_stride, _addr(master_host), _addr(m_host),
+                                 _addr(v_host), _addr(grad16_host), _addr(params16_host),
+                                 _addr(params), N, P, stage, t, lr, beta1, beta2, eps, mode,
+                                 cpu_threads, _stream(stream))
+    if rc:
+        raise ZeroError(rc, "zero_offload_step")

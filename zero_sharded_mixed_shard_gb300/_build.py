@@ -23,7 +23,10 @@ LIB = os.path.join(BUILD, "libzero_step.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
               "-Xptxas", "-v", "--expt-relaxed-constexpr"]
-CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra"]
+# host C++: IEEE binary32 with no multiply-add contraction (GCC contracts by
+# default on AArch64), sqrt without errno so the host Adam loops vectorise
+CXX_FLAGS = ["-O3", "-std=c++17", "-fPIC", "-Wall", "-Wextra", "-ffp-contract=off",
+             "-fno-math-errno", "-pthread"]
 
 
 def _nvcc() -> str:
@@ -78,7 +81,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if failed:
         raise RuntimeError("compilation failed:\n" + "\n".join(failed))
     tmp = LIB + ".tmp"
-    subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
+    subprocess.run([nvcc, *ARCH, "-shared", "-Xcompiler", "-pthread", "-o", tmp, *objs], check=True)
     os.replace(tmp, LIB)
     return LIB
 

@@ -29,6 +29,9 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <new>
+#include <thread>
+#include <type_traits>
 #include <utility>
 #include <vector>
 
@@ -939,6 +942,161 @@ extern "C" int zero_adam_step_bucketed(const void* grads_fp16, int64_t rank_stri
                                      params_fp16, P),
                           t, lr, beta1, beta2, eps, mode, stream);
         if (rc) return rc;
+    }
+    return ZERO_OK;
+}
+
+// ---------------------------------------------------------------------------
+// ZeRO-Offload: the GPU forms the gradient mean and sends it to the host as
+// fp16; a host function runs the CPU Adam of each shard in stream order and
+// the shard's fp16 weights are copied back into the gathered vector.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// Mean of the P ranks' gradients to fp16, V elements per thread per
+// iteration; uses StepArgs' g, stride, p (the fp16 output), n, head, P,
+// p_pow2 and inv_p.
+template <int V, int PT>
+__global__ void __launch_bounds__(kThreads) zero_reduce_fp16_kernel(const StepArgs a)
+{
+    const int P = PT > 0 ? PT : a.P;
+    const long long tid = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
+    const long long nthreads = static_cast<long long>(gridDim.x) * kThreads;
+    const long long body = (a.n - a.head) / V;
+    const long long tail_start = a.head + body * V;
+    auto one = [&](long long i, auto vtag) {
+        constexpr int W = decltype(vtag)::value;
+        float acc[W];
+#pragma unroll
+        for (int j = 0; j < W; ++j) acc[j] = 0.0f;
+        const __half* gp = a.g + i;
+#pragma unroll 8
+        for (int r = 0; r < P; ++r) accumulate<W>(acc, load_halves<W>(gp + static_cast<long long>(r) * a.stride));
+#pragma unroll
+        for (int j = 0; j < W; ++j) acc[j] = finish_mean<PT>(acc[j], a);
+        store_halves<W>(a.p + i, acc);
+    };
+    if (tid < a.head) one(tid, std::integral_constant<int, 1>{});
+    if (tid < a.n - tail_start) one(tail_start + tid, std::integral_constant<int, 1>{});
+    for (long long c = tid; c < body; c += nthreads) one(a.head + c * V, std::integral_constant<int, V>{});
+}
+
+KernelFn pick_reduce_kernel(int V, int P)
+{
+    if (V != 8) return zero_reduce_fp16_kernel<1, 0>;
+    switch (P) {
+    case 4: return zero_reduce_fp16_kernel<8, 4>;
+    case 8: return zero_reduce_fp16_kernel<8, 8>;
+    case 16: return zero_reduce_fp16_kernel<8, 16>;
+    case 32: return zero_reduce_fp16_kernel<8, 32>;
+    case 64: return zero_reduce_fp16_kernel<8, 64>;
+    default: return zero_reduce_fp16_kernel<8, 0>;
+    }
+}
+
+// The CPU update of every shard, run by the CUDA driver in stream order.
+// The shards are contiguous, so one dynamically scheduled pass of the host
+// threads over [0, N) updates every rank's shard ([P3] §2.3 gives each
+// GPU's shard to CPU workers); chunks go to whichever thread is free.
+struct OffloadUpdate {
+    const void* g16;
+    float* w;
+    float* m;
+    float* v;
+    void* p16;
+    int64_t N;
+    int64_t t;
+    float lr, b1, b2, eps;
+    int32_t mode;
+    int32_t threads;
+};
+
+void CUDART_CB offload_update(void* arg)
+{
+    OffloadUpdate* u = static_cast<OffloadUpdate*>(arg);
+    // the arguments were validated when the step was enqueued
+    (void)zero_cpu_adam(u->g16, u->w, u->m, u->v, u->p16, u->N, u->t, u->lr, u->b1, u->b2, u->eps, u->mode,
+                        u->threads);
+    delete u;
+}
+
+} // namespace
+
+extern "C" int zero_reduce_scatter_fp16(const void* grads_fp16, int64_t rank_stride, int64_t grad_offset,
+                                        int32_t P, int64_t n, void* out_fp16, void* cuda_stream)
+{
+    if (!grads_fp16 || !out_fp16 || n < 1 || P < 1 || P > ZERO_MAX_RANKS || grad_offset < 0) return ZERO_EINVAL;
+    if (P > 1 && rank_stride < n) return ZERO_EINVAL;
+    const uintptr_t gg = reinterpret_cast<uintptr_t>(grads_fp16), go = reinterpret_cast<uintptr_t>(out_fp16);
+    if (gg % 2 || go % 2) return ZERO_EALIGN;
+    const uintptr_t g_span = (static_cast<uintptr_t>(P - 1) * static_cast<uintptr_t>(rank_stride) +
+                              static_cast<uintptr_t>(grad_offset) + static_cast<uintptr_t>(n)) * 2;
+    if (overlaps(gg, g_span, go, static_cast<uintptr_t>(n) * 2)) return ZERO_EOVERLAP;
+    StepArgs a{};
+    a.g = static_cast<const __half*>(grads_fp16) + grad_offset;
+    a.stride = rank_stride;
+    a.p = static_cast<__half*>(out_fp16);
+    a.n = n;
+    a.P = P;
+    a.p_pow2 = (P & (P - 1)) == 0;
+    a.inv_p = 1.0f / static_cast<float>(P);
+    // 16-byte vectors when every rank's slice and the output share one phase
+    const uintptr_t ph = (reinterpret_cast<uintptr_t>(a.g) / 2) % 8;
+    const bool v8 = (P == 1 || rank_stride % 8 == 0) && (go / 2) % 8 == ph;
+    a.head = v8 ? static_cast<long long>((8 - ph) % 8) : 0;
+    if (a.head > n) a.head = n;
+    const int V = v8 ? 8 : 1;
+    KernelFn fn = pick_reduce_kernel(V, P);
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return record_cuda(cudaGetLastError());
+    const int per_sm = kernel_setup(fn, false);
+    if (per_sm < 0) return per_sm;
+    long long blocks = ((n - a.head) / V + kThreads - 1) / kThreads;
+    const long long cap = static_cast<long long>(sms) * per_sm;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    fn<<<static_cast<unsigned int>(blocks), kThreads, 0, static_cast<cudaStream_t>(cuda_stream)>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : record_cuda(e);
+}
+
+extern "C" int zero_offload_step(const void* grads_fp16, int64_t rank_stride, float* master_host, float* m_host,
+                                 float* v_host, void* grad16_host, void* params16_host, void* params_fp16,
+                                 int64_t N, int32_t P, int32_t stage, int64_t t, float lr, float beta1,
+                                 float beta2, float eps, int32_t mode, int32_t cpu_threads, void* cuda_stream)
+{
+    int rc = check_scalars(N, P, stage, t, lr, beta1, beta2, eps, mode);
+    if (rc) return rc;
+    if (rank_stride < N || cpu_threads < 0 || cpu_threads > 1024) return ZERO_EINVAL;
+    if (!grads_fp16 || !master_host || !m_host || !v_host || !grad16_host || !params16_host || !params_fp16)
+        return ZERO_EINVAL;
+    if (reinterpret_cast<uintptr_t>(master_host) % 4 || reinterpret_cast<uintptr_t>(m_host) % 4 ||
+        reinterpret_cast<uintptr_t>(v_host) % 4 || reinterpret_cast<uintptr_t>(params16_host) % 2 ||
+        reinterpret_cast<uintptr_t>(params_fp16) % 2)
+        return ZERO_EALIGN;
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    // the GPU side of every rank: the fp16 gradient mean lands in host memory
+    rc = zero_reduce_scatter_fp16(grads_fp16, rank_stride, 0, P, N, grad16_host, cuda_stream);
+    if (rc) return rc;
+    const int64_t M = N / P + (N % P != 0);
+    uint16_t* p16 = static_cast<uint16_t*>(params16_host);
+    OffloadUpdate* u = new (std::nothrow) OffloadUpdate{grad16_host, master_host, m_host, v_host, p16, N, t, lr,
+                                                        beta1, beta2, eps, mode, cpu_threads};
+    if (!u) return ZERO_ENOMEM;
+    cudaError_t ce = cudaLaunchHostFunc(stream, offload_update, u);
+    if (ce != cudaSuccess) {
+        delete u;
+        return record_cuda(ce);
+    }
+    // the all-gather: shard k's fp16 weights at offset kM of the device vector
+    __half* params = static_cast<__half*>(params_fp16);
+    for (int32_t k = 0; k < P; ++k) {
+        const int64_t b = static_cast<int64_t>(k) * M < N ? static_cast<int64_t>(k) * M : N;
+        const int64_t e = b + M < N ? b + M : N;
+        if (b >= e) continue;
+        ce = cudaMemcpyAsync(params + b, p16 + b, static_cast<size_t>(e - b) * 2, cudaMemcpyHostToDevice, stream);
+        if (ce != cudaSuccess) return record_cuda(ce);
     }
     return ZERO_OK;
 }
