@@ -66,6 +66,8 @@ def parse_args(argv=None):
                     help="priority of the step's stream in the overlap leg")
     ap.add_argument("--offload", action="store_true",
                     help="time the ZeRO-Offload step (update on the host CPU) instead")
+    ap.add_argument("--mlp4", action="store_true",
+                    help="time the layer-pipelined ZeRO-3 step of the 4-layer scalar MLP instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -641,6 +643,69 @@ def run_offload(args, wl, mode, dist):
     return 0
 
 
+def run_mlp4(args, dist):
+    """Training steps of the 4-layer scalar MLP on 4 simulated ranks (one
+    layer each), layer-pipelined on two streams and serial on one."""
+    import numpy as np
+    import torch
+
+    import zero_sharded_mixed_shard_gb300 as z
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(dist.local_rank)
+    dist.init("nccl")
+    P, n = 4, 256
+    rng = np.random.default_rng(0)
+    dev = torch.device("cuda", dist.local_rank)
+    master0 = torch.tensor([rng.uniform(0.6, 1.2) if i % 2 == 0 else rng.uniform(0.0, 0.2)
+                            for i in range(8)], dtype=torch.float32, device=dev)
+    x = torch.from_numpy(rng.uniform(0.1, 1.0, (P, n)).astype(np.float32)).to(dev)
+    main, side = torch.cuda.current_stream(dev), torch.cuda.Stream(dev)
+    reps = max(10, min(args.steps, 2000))
+    out = {}
+    for pipelined in (True, False):
+        master, m, v = master0.clone(), torch.zeros(8, device=dev), torch.zeros(8, device=dev)
+        shard16 = master0.half()
+        gathered16 = torch.zeros(8, dtype=torch.float16, device=dev)
+        grads16 = torch.zeros((P, 8), dtype=torch.float16, device=dev)
+        loss = torch.zeros(P, device=dev)
+        t = 0
+
+        def step():
+            nonlocal t
+            t += 1
+            z.zero_mlp4_zero3_step(x, P, n, gathered16, master, m, v, shard16, grads16, 8, loss, t,
+                                   1e-2, 0.9, 0.999, 1e-8, 0, pipelined=pipelined,
+                                   main_stream=main, step_stream=side)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        loss0 = float(loss.mean())
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h0 = time.perf_counter()
+        e0.record(main)
+        for _ in range(reps):
+            step()
+        e1.record(main)
+        torch.cuda.synchronize()
+        host_us = (time.perf_counter() - h0) * 1e6 / reps
+        out["pipelined" if pipelined else "serial"] = {
+            "us_per_step": e0.elapsed_time(e1) * 1e3 / reps, "host_enqueue_us_per_step": host_us,
+            "loss_after_warmup": loss0, "loss_at_end": float(loss.mean())}
+    if dist.rank == 0:
+        line = {"metric": "microseconds per training step, layer-pipelined ZeRO-3 (4-layer scalar MLP)",
+                "value": out["pipelined"]["us_per_step"], "unit": "us/step", "n_gpus": dist.world,
+                "steps": reps, "warmup": args.warmup, "higher_is_better": False, "dtype": "f32",
+                "data": "synthetic", "config": {"workload": f"mlp4: P={P} ranks, {n} samples each, "
+                                                            "one layer (w, b) per rank"},
+                "gpu_launches_per_step": 1 + 4 + 4 + 1, **out}
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     from zero_sharded_mixed_shard_gb300 import synth
@@ -653,6 +718,8 @@ def main(argv=None):
         return run_overlap(args, wl, mode, dist)
     if args.offload:
         return run_offload(args, wl, mode, dist)
+    if args.mlp4:
+        return run_mlp4(args, dist)
     return run_ours(args, wl, mode, dist)
 
 

@@ -309,6 +309,49 @@ int zero_offload_step(const void* grads_fp16, int64_t rank_stride, float* master
                       int64_t N, int32_t P, int32_t stage, int64_t t, float lr, float beta1,
                       float beta2, float eps, int32_t mode, int32_t cpu_threads, void* cuda_stream);
 
+/* ------------------------------------------------------------------------ */
+/* The layer-pipelined ZeRO-3 example: a 4-layer scalar MLP on P ranks      */
+/* ([P1] §（四）ZeRO-3 层间流水线优化).  Parameters in flat order            */
+/* (w1, b1, w2, b2, w3, b3, w4, b4); h_k = ReLU(w_k h_{k-1} + b_k), h_0 = x; */
+/* y = w4 h3 + b4; L = (y - x)^2 / 2.  x is device fp32 [P][n]: rank r's n  */
+/* samples; 1 <= P <= 8.                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* loss[r] = mean over rank r's samples of (y - x)^2 / 2, with the fp16
+ * parameters params_fp16 [8] (device).  Errors: ZERO_EINVAL, ZERO_ECUDA. */
+int zero_mlp4_loss(const void* params_fp16, const float* x, int32_t P, int32_t n, float* loss,
+                   void* cuda_stream);
+
+/* Rank r's mean gradient over its samples of layer `layer`'s (w, b)
+ * (1 <= layer <= 4), written as fp16 to grads_fp16[r * rank_stride +
+ * 2 (layer - 1) + {0, 1}] -- the backward formulas of [P1] §（四） 1., with
+ * the forward pass recomputed from x (no activations are kept).
+ * Errors: ZERO_EINVAL (rank_stride < 8, bad sizes), ZERO_ECUDA. */
+int zero_mlp4_layer_grads(int32_t layer, const void* params_fp16, const float* x, int32_t P,
+                          int32_t n, void* grads_fp16, int64_t rank_stride, void* cuda_stream);
+
+/* One ZeRO-3 training step with the page's layer pipeline
+ * ([P1] §（四） 2. 前向传播和反向传播的层间流水线并行执行):
+ *  - all-gather: the owners' fp16 shards shard_fp16 [8] are copied into the
+ *    gathered vector gathered_fp16 [8] that the pass reads;
+ *  - forward: loss[r] as zero_mlp4_loss;
+ *  - backward, layer 4 down to 1, on main_stream (zero_mlp4_layer_grads into
+ *    grads_fp16 [P][rank_stride]); as soon as the lowest layer of shard k
+ *    (M = ceil(8/P) parameters, ceil partition) is done, step_stream waits
+ *    for it and runs zero_adam_step_shard(k) (stage 3): reduce-scatter of the
+ *    shard's gradients to its owner, Adam on master / m / v [8] (the owners'
+ *    fp32 shards, concatenated) and the owner's fp16 shard written into
+ *    shard_fp16 -- while main_stream goes on with the lower layers.
+ *  pipelined = 0 puts everything on main_stream in the same order.  Before
+ *  returning, main_stream is made to wait for every update, so the next
+ *  step's all-gather sees them.  All buffers are device memory.
+ * Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
+int zero_mlp4_zero3_step(const float* x, int32_t P, int32_t n, void* gathered_fp16, float* master,
+                         float* m, float* v, void* shard_fp16, void* grads_fp16,
+                         int64_t rank_stride, float* loss, int64_t t, float lr, float beta1,
+                         float beta2, float eps, int32_t mode, int32_t pipelined,
+                         void* main_stream, void* step_stream);
+
 /* Bounded waits that gave up, over every step launched on the current
  * device since the last reset.  The fused kernels wait on shared-memory
  * barriers for their own bulk copies; each wait gives up after 2 seconds,

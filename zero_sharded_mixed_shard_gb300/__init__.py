@@ -32,7 +32,8 @@ MODE_FOLDED_STORAGE = 2
 EXPORTED = ("zero_init_layout", "zero_free_layout", "zero_shard_range", "zero_memory_bytes",
             "zero_adam_step", "zero_adam_step_shard", "zero_plan_buckets", "zero_adam_step_range",
             "zero_adam_step_bucketed", "zero_reduce_scatter_fp16", "zero_cpu_adam",
-            "zero_offload_step", "zero_device_timeouts",
+            "zero_offload_step", "zero_mlp4_loss", "zero_mlp4_layer_grads",
+            "zero_mlp4_zero3_step", "zero_device_timeouts",
             "zero_selftest_wait_timeout", "zero_strerror",
             "zero_last_cuda_error", "zero_last_cuda_error_string")
 
@@ -118,6 +119,13 @@ def lib() -> ctypes.CDLL:
     L.zero_offload_step.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, i64, i32, i32, i64,
                                     f32, f32, f32, f32, i32, i32, vp]
     L.zero_offload_step.restype = ctypes.c_int
+    L.zero_mlp4_loss.argtypes = [vp, vp, i32, i32, vp, vp]
+    L.zero_mlp4_loss.restype = ctypes.c_int
+    L.zero_mlp4_layer_grads.argtypes = [i32, vp, vp, i32, i32, vp, i64, vp]
+    L.zero_mlp4_layer_grads.restype = ctypes.c_int
+    L.zero_mlp4_zero3_step.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, i64,
+                                       f32, f32, f32, f32, i32, i32, vp, vp]
+    L.zero_mlp4_zero3_step.restype = ctypes.c_int
     L.zero_selftest_wait_timeout.argtypes = [vp, i64, vp, vp, vp, vp, i64, i32, i32, i64,
                                              f32, f32, f32, f32, i32, vp]
     L.zero_selftest_wait_timeout.restype = ctypes.c_int
@@ -332,3 +340,32 @@ def zero_offload_step(grads, rank_stride: int, master_host, m_host, v_host, grad
                                  cpu_threads, _stream(stream))
     if rc:
         raise ZeroError(rc, "zero_offload_step")
+
+
+def zero_mlp4_loss(params16, x, P: int, n: int, loss, stream=None) -> None:
+    rc = lib().zero_mlp4_loss(_addr(params16), _addr(x), P, n, _addr(loss), _stream(stream))
+    if rc:
+        raise ZeroError(rc, "zero_mlp4_loss")
+
+
+def zero_mlp4_layer_grads(layer: int, params16, x, P: int, n: int, grads16, rank_stride: int,
+                          stream=None) -> None:
+    rc = lib().zero_mlp4_layer_grads(layer, _addr(params16), _addr(x), P, n, _addr(grads16),
+                                     rank_stride, _stream(stream))
+    if rc:
+        raise ZeroError(rc, "zero_mlp4_layer_grads")
+
+
+def zero_mlp4_zero3_step(x, P: int, n: int, gathered16, master, m, v, shard16, grads16,
+                         rank_stride: int, loss, t: int, lr: float, beta1: float, beta2: float,
+                         eps: float, mode: int, pipelined: bool = True, main_stream=None,
+                         step_stream=None) -> None:
+    """Enqueue one layer-pipelined ZeRO-3 step of the 4-layer scalar MLP
+    (see include/zero_step.h)."""
+    rc = lib().zero_mlp4_zero3_step(_addr(x), P, n, _addr(gathered16), _addr(master), _addr(m),
+                                    _addr(v), _addr(shard16), _addr(grads16), rank_stride,
+                                    _addr(loss), t, lr, beta1, beta2, eps, mode,
+                                    1 if pipelined else 0, _stream(main_stream),
+                                    _stream(step_stream) if step_stream is not None else None)
+    if rc:
+        raise ZeroError(rc, "zero_mlp4_zero3_step")

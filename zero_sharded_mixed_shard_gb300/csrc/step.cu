@@ -1156,6 +1156,12 @@ extern "C" int zero_device_timeouts(int64_t* count, int32_t reset)
     return ZERO_OK;
 }
 
+// Used by the other translation units of the library (not exported).
+__attribute__((visibility("hidden"))) int zero_record_cuda_error(int err)
+{
+    return record_cuda(static_cast<cudaError_t>(err));
+}
+
 extern "C" int zero_last_cuda_error(void) { return g_last_cuda_error; }
 
 extern "C" const char* zero_last_cuda_error_string(void)
