@@ -47,6 +47,10 @@
  *  - fp32 -> fp16 rounds to nearest, ties to even; overflow gives +-inf;
  *    subnormal halves are kept.
  *  - No weight decay, clipping or loss scaling (the pages mention none).
+ *  - mode 3: plain SGD, w <- w - lr * g ([P1] §（一）; m and v untouched).
+ *    mode 4: SGD with momentum; [P3] §1.1.1 names it and its extra buffer
+ *    but prints no formula, so the plainest form: m <- b1 * m + g,
+ *    w <- w - lr * m (b1 plays the momentum coefficient; v untouched).
  */
 #include <float.h>
 #include <math.h>
@@ -210,6 +214,17 @@ static void adam_update(const step_scalars* s, const float* g, float* w, float* 
             v_new = (s->b2 * v[j] + s->omb2 * gg) / s->bc2;
             m_hat = m_new;
             v_hat = v_new;
+        } else if (s->mode == 3) {
+            /* plain SGD ([P1] §（一）): w <- w - lr * g; no moments */
+            w[j] = w[j] - s->lr * gj;
+            continue;
+        } else if (s->mode == 4) {
+            /* SGD with momentum ([P3] §1.1.1 names it and its extra buffer, no
+             * formula): m <- beta1 * m + g, w <- w - lr * m */
+            m_new = s->b1 * m[j] + gj;
+            w[j] = w[j] - s->lr * m_new;
+            m[j] = m_new;
+            continue;
         } else {
             /* folded storage: undo the previous step's correction, advance the
              * raw average, store the corrected value */
@@ -296,7 +311,7 @@ static int threaded_range_step(const uint16_t* grads, int64_t rank_stride, int32
 
 static int check_common(int32_t P, int64_t t, int mode)
 {
-    if (P < 1 || t < 1 || mode < 0 || mode > 2) return -2;
+    if (P < 1 || t < 1 || mode < 0 || mode > 4) return -2;
     return 0;
 }
 
@@ -405,6 +420,15 @@ int oracle_adam_elems_f64(const uint16_t* grads, int64_t rank_stride, int32_t P,
             acc += (double)oracle_half_to_float(grads[(int64_t)r * rank_stride + j]);
         const double g = acc / (double)P;
         double m_new, v_new, m_hat, v_hat;
+        if (mode == 3) {
+            w[j] = w[j] - lr * g;
+            continue;
+        }
+        if (mode == 4) {
+            m[j] = b1 * m[j] + g;
+            w[j] = w[j] - lr * m[j];
+            continue;
+        }
         if (mode == 0) {
             m_new = b1 * m[j] + (1.0 - b1) * g;
             v_new = b2 * v[j] + (1.0 - b2) * g * g;

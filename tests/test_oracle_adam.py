@@ -297,3 +297,54 @@ def test_offload_differs_from_fused_only_through_the_gradient_rounding(oracle_mo
     p1, _ = oracle_mod.offload_elems(codes, n, P, *a, 1, 1e-3, 0.9, 0.999, 1e-8, 0)
     p2 = oracle_mod.adam_elems(codes, n, P, *b, 1, 1e-3, 0.9, 0.999, 1e-8, 0)
     assert np.array_equal(p1, p2)
+
+
+# ---------------------------------------------------------------------------
+# the other optimizers the pages name: plain SGD (深度学习专题：模型训练的数据并行
+# （三） §（一）) and SGD with momentum (ZeRO 技术原理：进阶与 Offload §1.1.1)
+# ---------------------------------------------------------------------------
+
+def test_sgd_steps_and_independence_of_t(oracle_mod):
+    g = np.array([1e-3, -2e-3, 0.5, -0.25, 3e-5], np.float16).astype(np.float64)
+    n, T = g.size, 40
+    w0 = np.full(n, 0.75, np.float32)
+    w, m, v = w0.copy(), np.full(n, 7.0, np.float32), np.full(n, 9.0, np.float32)
+    for t in range(1, T + 1):
+        run(oracle_mod, g[None, :], w, m, v, t, 3)
+    expect = w0.astype(np.float64) - T * f64(LR) * g
+    assert np.all(np.abs(w - expect) <= T * np.spacing(np.float32(0.75)) + T * np.abs(g) * 1e-6)
+    assert np.all(m == 7.0) and np.all(v == 9.0)              # no moments in plain SGD
+    # the step does not depend on t (no bias correction)
+    a, b = w0.copy(), w0.copy()
+    run(oracle_mod, g[None, :], a, m, v, 1, 3)
+    run(oracle_mod, g[None, :], b, m, v, 1000, 3)
+    assert np.array_equal(a, b)
+
+
+def test_momentum_geometric_series(oracle_mod):
+    # constant g from m = 0: m_t = g (1 - mu^t) / (1 - mu); w_T = w0 - lr sum_t m_t
+    g = np.array([1e-3, -2e-3, 0.5, -0.25], np.float16).astype(np.float64)
+    n, T, mu = g.size, 25, f64(B1)
+    w0 = np.full(n, 0.5, np.float32)
+    w, m, v = w0.copy(), np.zeros(n, np.float32), np.full(n, 3.0, np.float32)
+    for t in range(1, T + 1):
+        run(oracle_mod, g[None, :], w, m, v, t, 4)
+    m_exp = g * (1 - mu ** T) / (1 - mu)
+    assert np.allclose(m, m_exp, rtol=1e-5, atol=0)
+    s = sum((1 - mu ** t) / (1 - mu) for t in range(1, T + 1))
+    expect = w0.astype(np.float64) - f64(LR) * g * s
+    assert np.all(np.abs(w - expect) <= T * np.spacing(np.float32(0.5)) + np.abs(g) * s * 1e-4)
+    assert np.all(v == 3.0)
+
+
+def test_momentum_two_steps_by_hand(oracle_mod):
+    # m1 = g1 exactly; m2 = mu g1 + g2; w2 = w0 - lr g1 - lr (mu g1 + g2)
+    w0 = np.full(G1.size, 0.25, np.float32)
+    w, m, v = w0.copy(), np.zeros(G1.size, np.float32), np.zeros(G1.size, np.float32)
+    run(oracle_mod, G1[None, :], w, m, v, 1, 4)
+    assert np.array_equal(m, G1.astype(np.float32))
+    run(oracle_mod, G2[None, :], w, m, v, 2, 4)
+    mu, lr = f64(B1), f64(LR)
+    assert np.allclose(m, mu * G1 + G2, rtol=1e-6, atol=1e-12)
+    expect = w0.astype(np.float64) - lr * G1 - lr * (mu * G1 + G2)
+    assert np.all(np.abs(w - expect) <= 3 * np.spacing(np.float32(0.25)))

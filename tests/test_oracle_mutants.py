@@ -35,6 +35,9 @@ MUTANTS = {
                            "ldexpf((float)(1024 + frac), expo - 24)"),
     "all-gather offset": ("memcpy(params + begin, shard_half", "memcpy(params + begin / 2, shard_half"),
     "offload gradient not rounded": ("g[j] = oracle_half_to_float(h);", "(void)h;"),
+    "sgd sign": ("w[j] = w[j] - s->lr * gj;\n            continue;", "w[j] = w[j] + s->lr * gj;\n            continue;"),
+    "momentum without mu": ("m_new = s->b1 * m[j] + gj;", "m_new = m[j] + gj;"),
+    "momentum steps with g": ("w[j] = w[j] - s->lr * m_new;", "w[j] = w[j] - s->lr * gj;"),
     "last shard loses its clamped tail": ("const int64_t end = begin + M < N ? begin + M : N;",
                                           "const int64_t end = begin + M < N ? begin + M : N - 1;"),
 }
