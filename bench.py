@@ -254,6 +254,7 @@ def oracle_rate(wl, mode: int, budget_s: float, sample: int | None = None, steps
 
 def run_reference(args, wl, mode, dist):
     """--impl reference: the CPU oracle on the same workload, rank 0 only."""
+    from zero_sharded_mixed_shard_gb300 import synth
     if dist.rank != 0:
         return 0
     # size each step's sample so the whole run stays within ~90 s of host time
@@ -272,7 +273,7 @@ def run_reference(args, wl, mode, dist):
         "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(timed), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(wl, mode, sample_note=f"first {sample} elements per step"),
-        "achieved_gbs": value * wl.bytes_per_elem / 1e9,
+        "achieved_gbs": value * synth.bytes_per_elem(wl.P, mode) / 1e9,
         "cpu_baseline": {"value": value, "unit": "params/s", "cores": cores, "kind": "oracle",
                          "sample": f"elements [0, {sample}) of the {wl.name} workload, all "
                                    f"{wl.P} ranks, one oracle call per step"},
@@ -284,12 +285,14 @@ def run_reference(args, wl, mode, dist):
 
 
 def workload_config(wl, mode, sample_note=None):
+    from zero_sharded_mixed_shard_gb300 import synth
     cfg = {"workload": f"{wl.name}: N={wl.N:,} P={wl.P} ZeRO-{wl.stage} "
                        f"{'shard ' + str(wl.shard) + ' only, ' if wl.shard is not None else ''}"
                        f"Adam mode {mode}",
            "N": wl.N, "elements_per_step": wl.elems, "P": wl.P, "stage": wl.stage, "mode": mode,
-           "rank_stride": wl.rank_stride(True), "bytes_per_elem": wl.bytes_per_elem,
-           "l2": f"inputs larger than L2: {wl.elems * wl.bytes_per_elem / 1e9:.2f} GB moved per step"}
+           "rank_stride": wl.rank_stride(True), "bytes_per_elem": synth.bytes_per_elem(wl.P, mode),
+           "l2": f"inputs larger than L2: {wl.elems * synth.bytes_per_elem(wl.P, mode) / 1e9:.2f} "
+                 "GB moved per step"}
     if sample_note:
         cfg["sample"] = sample_note
     return cfg
@@ -358,7 +361,7 @@ def run_ours(args, wl, mode, dist):
 
     elems_total = E * K * dist.world
     value = elems_total / (region_ms / 1e3)
-    alg_bytes = E * wl.bytes_per_elem
+    alg_bytes = E * synth.bytes_per_elem(P, mode)
     achieved = alg_bytes / (mean_launch_ms / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
 

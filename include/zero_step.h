@@ -62,6 +62,9 @@ extern "C" {
 #define ZERO_MODE_STANDARD 0       /* m, v are raw moving averages; bias-corrected in the update */
 #define ZERO_MODE_FOLDED_LITERAL 1 /* [P1] §（一） as printed: recursion on the divided m, v */
 #define ZERO_MODE_FOLDED_STORAGE 2 /* stored m, v are bias-corrected; recursion on the raw average */
+#define ZERO_MODE_SGD 3            /* [P1] §（一）: w <- w - lr g; m and v unused (may be NULL) */
+#define ZERO_MODE_MOMENTUM 4       /* [P3] §1.1.1 SGD with momentum: m <- beta1 m + g, w <- w - lr m;
+                                      v unused (may be NULL) */
 
 /* ------------------------------------------------------------------------ */
 /* Layout table (host only, no CUDA)                                        */
@@ -150,8 +153,13 @@ int zero_memory_bytes(int64_t N, int32_t P, int32_t stage, double* bytes_mixed,
  *  t            1-based index of the update being produced (first step: 1).
  *  lr, beta1, beta2, eps   Adam hyper-parameters; finite, 0 <= beta < 1,
  *               eps >= 0 ([P1] §（一）: eps is added outside the sqrt).
- *  mode         ZERO_MODE_STANDARD, ZERO_MODE_FOLDED_LITERAL or
- *               ZERO_MODE_FOLDED_STORAGE.
+ *  mode         ZERO_MODE_STANDARD, ZERO_MODE_FOLDED_LITERAL,
+ *               ZERO_MODE_FOLDED_STORAGE (Adam: master, m, v), ZERO_MODE_SGD
+ *               (master only: m and v are neither read nor written and may
+ *               be NULL) or ZERO_MODE_MOMENTUM (master and m; v may be NULL;
+ *               beta1 is the momentum coefficient, beta2 and eps are only
+ *               validated).  Bytes moved per element: 2P + 26 for Adam,
+ *               2P + 18 with momentum, 2P + 10 for plain SGD.
  *
  * Per element i, every operation a separately rounded fp32 operation
  * (no contraction), in this order:
@@ -162,6 +170,8 @@ int zero_memory_bytes(int64_t N, int32_t P, int32_t stage, double* bytes_mixed,
  *   mode 2: with bp = fp32(1 - beta^(t-1)):
  *           m = (b1*(m*bp1) + (1-b1)*g)/bc1;  v = (b2*(v*bp2) + (1-b2)*(g*g))/bc2
  *   master = master - lr * (mh / (sqrt(vh) + eps));  params[i] = fp16_rne(master)
+ *   mode 3: master = master - lr * g
+ *   mode 4: m = b1*m + g;  master = master - lr * m
  *
  * Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_EOVERLAP (any two of master, m, v,
  * params overlap, or one of them overlaps the gradient span), ZERO_ECUDA.

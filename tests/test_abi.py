@@ -70,8 +70,8 @@ def _call(zlib, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(grads=None), -1), (dict(master=None), -1), (dict(m=None), -1), (dict(v=None), -1),
     (dict(params=None), -1), (dict(N=0), -1), (dict(N=-5), -1), (dict(P=0), -1),
-    (dict(P=1025), -1), (dict(stage=4), -1), (dict(stage=-1), -1), (dict(mode=3), -1),
-    (dict(mode=-1), -1), (dict(t=0), -1), (dict(lr=math.nan), -1), (dict(lr=math.inf), -1),
+    (dict(P=1025), -1), (dict(stage=4), -1), (dict(stage=-1), -1), (dict(mode=7), -1),
+    (dict(mode=-1), -1), (dict(mode=5), -1), (dict(t=0), -1), (dict(lr=math.nan), -1), (dict(lr=math.inf), -1),
     (dict(beta1=1.0), -1), (dict(beta2=-0.5), -1), (dict(eps=-1e-8), -1),
     (dict(eps=math.inf), -1), (dict(rank_stride=999), -1),
     (dict(master=W + 2), -2), (dict(v=V + 1), -2), (dict(params=PP + 1), -2),
@@ -140,3 +140,16 @@ def test_range_and_bucketed_reject(zlib):
     arr[0].begin, arr[0].end = 0, 1000
     assert L.zero_adam_step_bucketed(G, 1000, W + 2, MM, V, PP, 1000, 4, 2, 1, 1e-3, 0.9, 0.999,
                                      1e-8, 0, arr, 1, None, 0) == zlib.ZERO_EALIGN
+
+
+@no_gpu
+def test_unused_state_may_be_null_but_used_state_may_not(zlib):
+    # SGD (mode 3) uses neither m nor v; momentum (mode 4) uses m; Adam both.
+    # Only the rejected calls are made here: nothing reaches a kernel.
+    assert _call(zlib, mode=4, m=None) == zlib.ZERO_EINVAL
+    assert _call(zlib, mode=0, v=None) == zlib.ZERO_EINVAL
+    assert _call(zlib, mode=3, master=None) == zlib.ZERO_EINVAL
+    # an unused buffer is not checked for alignment or overlap either: the
+    # first failing check is then on a used one
+    assert _call(zlib, mode=3, m=W + 1, v=W, params=PP + 1) == zlib.ZERO_EALIGN
+    assert _call(zlib, mode=4, v=MM + 1, m=W + 8) == zlib.ZERO_EOVERLAP

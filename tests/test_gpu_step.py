@@ -295,7 +295,7 @@ def test_validation_with_device_buffers(z):
     g = torch.zeros((P, N), dtype=torch.float16, device="cuda")
     s = dev_state(*synth.np_state(N, 1))
     before = host_state(s)
-    bad = [dict(N=0), dict(P=0), dict(t=0), dict(mode=3), dict(stage=7), dict(beta1=1.0),
+    bad = [dict(N=0), dict(P=0), dict(t=0), dict(mode=5), dict(stage=7), dict(beta1=1.0),
            dict(eps=-1.0), dict(rank_stride=N - 1)]
     for kw in bad:
         a = dict(rank_stride=N, N=N, P=P, stage=2, t=1, beta1=B1, eps=EPS, mode=0)
@@ -391,3 +391,37 @@ def test_tma_and_vector_paths_agree(z):
     gpu_step(z, g, stride, b, N, P, 2, 0)
     for x, y in zip(host_state(a), host_state(b)):
         assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+# ---------------------------------------------------------------------------
+# the other optimizers the pages name: plain SGD and SGD with momentum
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", [3, 4])
+@pytest.mark.parametrize("big", [False, True])
+def test_sgd_and_momentum_match_oracle(z, mode, big):
+    """Both kernels (vector path for the small problem, bulk pipeline for the
+    large one); the unused state is passed as NULL in odd steps and as a
+    sentinel-filled buffer, which must stay untouched, in even steps."""
+    P = 8
+    N = (torch.cuda.get_device_properties(0).multi_processor_count * 2048 * 4 + 13) if big else 50_001
+    stride = synth.round_up(N, 8)
+    w0, m0, v0, p0 = synth.np_state(N, 30 + mode)
+    m0 = (np.random.default_rng(1).standard_normal(N) * 1e-3).astype(np.float32)
+    ref = [w0.copy(), m0.copy(), v0.copy()]
+    s = dev_state(w0, m0, v0, p0)
+    sentinel = torch.full((N,), 1234.5, device="cuda")
+    for t in range(1, 5):
+        codes = synth.np_grads(P, N, stride, 1e-3, 500 + t, heavy_tail_frac=0.01)
+        pass_null = t % 2 == 1
+        m_arg = s[1] if mode == 4 else (None if pass_null else sentinel)
+        v_arg = None if pass_null else sentinel
+        z.zero_adam_step(dev_u16(codes), stride, s[0], m_arg, v_arg, s[3], N, P, 2, t, LR, B1, B2,
+                         EPS, mode)
+        p_ref = oracle.adam_elems(codes, stride, P, *ref, t, LR, B1, B2, EPS, mode, threads=8)
+        got = host_state(s)
+        assert max_ulps([got[0], got[1] if mode == 4 else ref[1], ref[2], got[3]],
+                        ref + [p_ref]) == (0, 0), (mode, big, t)
+    assert bool((sentinel == 1234.5).all())
+    if mode == 3:
+        assert np.array_equal(host_state(s)[1], m0)        # m untouched by plain SGD

@@ -27,6 +27,8 @@ ZERO_MAX_RANKS = 1024
 MODE_STANDARD = 0
 MODE_FOLDED_LITERAL = 1
 MODE_FOLDED_STORAGE = 2
+MODE_SGD = 3
+MODE_MOMENTUM = 4
 
 # every symbol include/zero_step.h declares
 EXPORTED = ("zero_init_layout", "zero_free_layout", "zero_shard_range", "zero_memory_bytes",

@@ -105,12 +105,29 @@ __device__ __forceinline__ float div_rn(float x, float d)
     return __fdiv_rn(x, d);
 }
 
+// The state streams a mode reads and writes: Adam all three, SGD with
+// momentum master and m, plain SGD master only.
+constexpr bool uses_m(int mode) { return mode != ZERO_MODE_SGD; }
+constexpr bool uses_v(int mode) { return mode <= ZERO_MODE_FOLDED_STORAGE; }
+constexpr int state_rows(int mode) { return 1 + (uses_m(mode) ? 1 : 0) + (uses_v(mode) ? 1 : 0); }
+
 // Adam on one element; w, m, v updated in place.  G = 1 takes the shortcuts
 // above for infinite operands, G = 0 calls the rounded intrinsics directly
 // (same results; only the speed on infinite operands differs).
 template <int MODE, int G = 1>
 __device__ __forceinline__ void adam_elem(const StepArgs& a, float g, float& w, float& m, float& v)
 {
+    if constexpr (MODE == ZERO_MODE_SGD) {
+        // w <- w - lr * g (深度学习专题：模型训练的数据并行（三） §（一）)
+        w = __fsub_rn(w, __fmul_rn(a.lr, g));
+        return;
+    } else if constexpr (MODE == ZERO_MODE_MOMENTUM) {
+        // m <- b1 * m + g, w <- w - lr * m
+        const float mn = __fadd_rn(__fmul_rn(a.b1, m), g);
+        w = __fsub_rn(w, __fmul_rn(a.lr, mn));
+        m = mn;
+        return;
+    }
     const float gg = __fmul_rn(g, g);
     float m_new, v_new, m_hat, v_hat;
     if constexpr (MODE == ZERO_MODE_STANDARD) {
@@ -253,10 +270,10 @@ __device__ __forceinline__ void step_elems(const StepArgs& a, long long i)
 {
     const int P = PT > 0 ? PT : a.P;
     // state loads first so they are in flight with the gradient loads
-    float w[V], m[V], v[V];
+    float w[V], m[V] = {}, v[V] = {};
     load_floats<V>(a.w + i, w);
-    load_floats<V>(a.m + i, m);
-    load_floats<V>(a.v + i, v);
+    if constexpr (uses_m(MODE)) load_floats<V>(a.m + i, m);
+    if constexpr (uses_v(MODE)) load_floats<V>(a.v + i, v);
 
     // reduce-scatter (own slice): fp32 sum in rank order 0..P-1 from +0
     float acc[V];
@@ -287,8 +304,8 @@ __device__ __forceinline__ void step_elems(const StepArgs& a, long long i)
         adam_elem<MODE>(a, g, w[j], m[j], v[j]);
     }
     store_floats<V>(a.w + i, w);
-    store_floats<V>(a.m + i, m);
-    store_floats<V>(a.v + i, v);
+    if constexpr (uses_m(MODE)) store_floats<V>(a.m + i, m);
+    if constexpr (uses_v(MODE)) store_floats<V>(a.v + i, v);
     store_halves<V>(a.p + i, w); // all-gather: element i of the full vector
 }
 
@@ -451,8 +468,8 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
 
     const __half* g0 = a.g + a.head;
     float* w0 = a.w + a.head;
-    float* m0 = a.m + a.head;
-    float* v0 = a.v + a.head;
+    float* m0 = uses_m(MODE) ? a.m + a.head : nullptr;
+    float* v0 = uses_v(MODE) ? a.v + a.head : nullptr;
     __half* p0 = a.p + a.head;
 
     auto tile_of = [&](long long u) { return blockIdx.x + (u / nch) * gridDim.x; };
@@ -465,21 +482,21 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
         const uint32_t hb = static_cast<uint32_t>(len) * 2, fb = static_cast<uint32_t>(len) * 4;
         unsigned char* st = smem + static_cast<size_t>(s) * kStageBytes;
         const uint32_t poison = (u == 0 && blockIdx.x == 0) ? a.poison_tx : 0u;
-        mbar_arrive_expect_tx(&full[s], hb * rc + (c == 0 ? 3 * fb : 0) + poison);
+        mbar_arrive_expect_tx(&full[s], hb * rc + (c == 0 ? state_rows(MODE) * fb : 0) + poison);
         const __half* src = g0 + static_cast<long long>(c) * kChunkRanks * a.stride + i0;
         for (int q = 0; q < rc; ++q)
             bulk_load(st + static_cast<size_t>(q) * kTile * 2, src + q * a.stride, hb, &full[s], policy);
         if (c == 0) {
             bulk_load(st + kGradBytes, w0 + i0, fb, &full[s], policy);
-            bulk_load(st + kGradBytes + kTile * 4, m0 + i0, fb, &full[s], policy);
-            bulk_load(st + kGradBytes + 2 * kTile * 4, v0 + i0, fb, &full[s], policy);
+            if constexpr (uses_m(MODE)) bulk_load(st + kGradBytes + kTile * 4, m0 + i0, fb, &full[s], policy);
+            if constexpr (uses_v(MODE)) bulk_load(st + kGradBytes + 2 * kTile * 4, v0 + i0, fb, &full[s], policy);
         }
     };
 
     if (tid == 0)
         for (long long u = 0; u < kStages && u < units; ++u) issue(u);
 
-    float acc[E], w[E], m[E], v[E];
+    float acc[E], w[E], m[E] = {}, v[E] = {};
     long long u = 0;
     bool failed = false;
     for (; u < units; ++u) {
@@ -502,8 +519,8 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
 #pragma unroll
                 for (int j = 0; j < E; ++j) acc[j] = 0.0f;
                 smem_floats<E>(st + kGradBytes + e0 * 4, w);
-                smem_floats<E>(st + kGradBytes + kTile * 4 + e0 * 4, m);
-                smem_floats<E>(st + kGradBytes + 2 * kTile * 4 + e0 * 4, v);
+                if constexpr (uses_m(MODE)) smem_floats<E>(st + kGradBytes + kTile * 4 + e0 * 4, m);
+                if constexpr (uses_v(MODE)) smem_floats<E>(st + kGradBytes + 2 * kTile * 4 + e0 * 4, v);
             }
             // ranks c*8 .. c*8+rc-1 of this tile, in rank order
             const int rc = P - c * kChunkRanks < kChunkRanks ? P - c * kChunkRanks : kChunkRanks;
@@ -516,7 +533,8 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
 #pragma unroll
                 for (int j = 0; j < E; ++j) {
                     gm[j] = finish_mean<PT>(acc[j], a);
-                    special |= !(isfinite(gm[j]) && isfinite(m[j]) && isfinite(v[j]));
+                    if constexpr (MODE <= ZERO_MODE_FOLDED_STORAGE) // the only modes that divide
+                        special |= !(isfinite(gm[j]) && isfinite(m[j]) && isfinite(v[j]));
                 }
                 // G = 2: the shortcuts for infinite operands are taken only by warps
                 // that hold a non-finite gradient mean or moment (one warp-uniform
@@ -530,8 +548,8 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
                 }
                 const long long i = i0 + e0;
                 store_floats<E>(w0 + i, w);
-                store_floats<E>(m0 + i, m);
-                store_floats<E>(v0 + i, v);
+                if constexpr (uses_m(MODE)) store_floats<E>(m0 + i, m);
+                if constexpr (uses_v(MODE)) store_floats<E>(v0 + i, v);
                 store_halves<E>(p0 + i, w); // all-gather: element head + i of the full vector
             }
         }
@@ -596,6 +614,8 @@ KernelFn pick_kernel(int mode, int V, int P)
     switch (mode) {
     case ZERO_MODE_STANDARD: return pick_v<ZERO_MODE_STANDARD>(V, P);
     case ZERO_MODE_FOLDED_LITERAL: return pick_v<ZERO_MODE_FOLDED_LITERAL>(V, P);
+    case ZERO_MODE_SGD: return pick_v<ZERO_MODE_SGD>(V, P);
+    case ZERO_MODE_MOMENTUM: return pick_v<ZERO_MODE_MOMENTUM>(V, P);
     default: return pick_v<ZERO_MODE_FOLDED_STORAGE>(V, P);
     }
 }
@@ -639,6 +659,8 @@ TmaKernel pick_tma_kernel(int mode, int P)
     switch (mode) {
     case ZERO_MODE_STANDARD: return pick_tma_p<ZERO_MODE_STANDARD>(P);
     case ZERO_MODE_FOLDED_LITERAL: return pick_tma_p<ZERO_MODE_FOLDED_LITERAL>(P);
+    case ZERO_MODE_SGD: return pick_tma_p<ZERO_MODE_SGD>(P);
+    case ZERO_MODE_MOMENTUM: return pick_tma_p<ZERO_MODE_MOMENTUM>(P);
     default: return pick_tma_p<ZERO_MODE_FOLDED_STORAGE>(P);
     }
 }
@@ -646,7 +668,7 @@ TmaKernel pick_tma_kernel(int mode, int P)
 // Widest vector V in {8,4,2,1} for which one head length h makes every
 // stream's element h start on a V-element boundary (at most 16 bytes per
 // access, so fp32 streams need min(V,4)-element alignment).
-int pick_vector(const StepArgs& a, long long* head)
+int pick_vector(const StepArgs& a, int mode, long long* head)
 {
     const uintptr_t g = reinterpret_cast<uintptr_t>(a.g) / 2;
     const uintptr_t p = reinterpret_cast<uintptr_t>(a.p) / 2;
@@ -658,7 +680,9 @@ int pick_vector(const StepArgs& a, long long* head)
         const uintptr_t ph = g % V;
         if (p % V != ph) continue;
         const int fv = V < 4 ? V : 4;
-        if (w % fv != ph % fv || m % fv != ph % fv || v % fv != ph % fv) continue;
+        if (w % fv != ph % fv) continue;
+        if (uses_m(mode) && m % fv != ph % fv) continue;
+        if (uses_v(mode) && v % fv != ph % fv) continue;
         long long h = static_cast<long long>((V - ph) % V);
         *head = h < a.n ? h : a.n;
         return V;
@@ -726,7 +750,7 @@ int check_scalars(int64_t N, int32_t P, int32_t stage, int64_t t, float lr, floa
 {
     if (N < 1 || P < 1 || P > ZERO_MAX_RANKS) return ZERO_EINVAL;
     if (stage < 0 || stage > 3) return ZERO_EINVAL;
-    if (mode < 0 || mode > 2) return ZERO_EINVAL;
+    if (mode < 0 || mode > ZERO_MODE_MOMENTUM) return ZERO_EINVAL;
     if (t < 1) return ZERO_EINVAL;
     if (!finite(lr) || !finite(b1) || !finite(b2) || !finite(eps)) return ZERO_EINVAL;
     if (!(b1 >= 0.0f && b1 < 1.0f) || !(b2 >= 0.0f && b2 < 1.0f) || !(eps >= 0.0f)) return ZERO_EINVAL;
@@ -735,22 +759,32 @@ int check_scalars(int64_t N, int32_t P, int32_t stage, int64_t t, float lr, floa
 
 // Validate the buffers of the range described by `a` (n >= 1) and fill in
 // the step scalars; *V and the head are chosen from the buffers' alignment.
-int prepare_range(StepArgs& a, int64_t t, float lr, float b1, float b2, float eps, int* V)
+int prepare_range(StepArgs& a, int64_t t, float lr, float b1, float b2, float eps, int mode, int* V)
 {
-    if (!a.g || !a.w || !a.m || !a.v || !a.p) return ZERO_EINVAL;
+    const bool um = uses_m(mode), uv = uses_v(mode);
+    if (!a.g || !a.w || !a.p || (um && !a.m) || (uv && !a.v)) return ZERO_EINVAL;
+    if (!um) a.m = nullptr; // a stream the mode does not use is never touched
+    if (!uv) a.v = nullptr;
     if (a.P > 1 && a.stride < a.n) return ZERO_EINVAL; // rank slices must not overlap
-    const uintptr_t gw = reinterpret_cast<uintptr_t>(a.w), gm = reinterpret_cast<uintptr_t>(a.m),
-                    gv = reinterpret_cast<uintptr_t>(a.v), gp = reinterpret_cast<uintptr_t>(a.p),
-                    gg = reinterpret_cast<uintptr_t>(a.g);
-    if (gw % 4 || gm % 4 || gv % 4 || gp % 2 || gg % 2) return ZERO_EALIGN;
+    const uintptr_t gg = reinterpret_cast<uintptr_t>(a.g);
+    if (reinterpret_cast<uintptr_t>(a.w) % 4 || reinterpret_cast<uintptr_t>(a.p) % 2 || gg % 2 ||
+        reinterpret_cast<uintptr_t>(a.m) % 4 || reinterpret_cast<uintptr_t>(a.v) % 4)
+        return ZERO_EALIGN;
+    // the outputs the mode writes must not overlap each other or the gradients
     const uintptr_t fb = static_cast<uintptr_t>(a.n) * 4, hb = static_cast<uintptr_t>(a.n) * 2;
     const uintptr_t g_span = (static_cast<uintptr_t>(a.P - 1) * static_cast<uintptr_t>(a.stride) +
                               static_cast<uintptr_t>(a.n)) * 2;
-    if (overlaps(gw, fb, gm, fb) || overlaps(gw, fb, gv, fb) || overlaps(gm, fb, gv, fb) ||
-        overlaps(gw, fb, gp, hb) || overlaps(gm, fb, gp, hb) || overlaps(gv, fb, gp, hb) ||
-        overlaps(gg, g_span, gw, fb) || overlaps(gg, g_span, gm, fb) || overlaps(gg, g_span, gv, fb) ||
-        overlaps(gg, g_span, gp, hb))
-        return ZERO_EOVERLAP;
+    uintptr_t out[4][2];
+    int n_out = 0;
+    out[n_out][0] = reinterpret_cast<uintptr_t>(a.w), out[n_out++][1] = fb;
+    out[n_out][0] = reinterpret_cast<uintptr_t>(a.p), out[n_out++][1] = hb;
+    if (um) out[n_out][0] = reinterpret_cast<uintptr_t>(a.m), out[n_out++][1] = fb;
+    if (uv) out[n_out][0] = reinterpret_cast<uintptr_t>(a.v), out[n_out++][1] = fb;
+    for (int i = 0; i < n_out; ++i) {
+        if (overlaps(gg, g_span, out[i][0], out[i][1])) return ZERO_EOVERLAP;
+        for (int j = i + 1; j < n_out; ++j)
+            if (overlaps(out[i][0], out[i][1], out[j][0], out[j][1])) return ZERO_EOVERLAP;
+    }
 
     // step scalars: bias corrections in double from the fp32 betas, rounded once
     a.lr = lr;
@@ -768,7 +802,7 @@ int prepare_range(StepArgs& a, int64_t t, float lr, float b1, float b2, float ep
     a.poison_tx = 0;
 
     long long head = 0;
-    *V = pick_vector(a, &head);
+    *V = pick_vector(a, mode, &head);
     a.head = head;
     return ZERO_OK;
 }
@@ -813,7 +847,7 @@ int launch_range(StepArgs a, int64_t t, float lr, float b1, float b2, float eps,
                  cudaStream_t stream)
 {
     int V = 1;
-    int rc = prepare_range(a, t, lr, b1, b2, eps, &V);
+    int rc = prepare_range(a, t, lr, b1, b2, eps, mode, &V);
     if (rc) return rc;
     const int sms = sm_count_of_current_device();
     if (sms <= 0) return record_cuda(cudaGetLastError());
@@ -860,7 +894,7 @@ extern "C" int zero_adam_step_shard(const void* grads_fp16, int64_t rank_stride,
     // a trailing rank that owns nothing: no buffer is touched, so none is
     // examined (zero-length allocations are often NULL)
     if (len == 0) return ZERO_OK;
-    if (!grads_fp16 || !master_s || !m_s || !v_s || !params_out) return ZERO_EINVAL;
+    if (!grads_fp16 || !master_s || !params_out) return ZERO_EINVAL; // m_s, v_s: checked by mode
     StepArgs a{};
     a.g = static_cast<const __half*>(grads_fp16) + grad_offset;
     a.stride = rank_stride;
@@ -883,8 +917,8 @@ StepArgs range_args(const void* grads_fp16, int64_t rank_stride, int64_t begin, 
     a.g = static_cast<const __half*>(grads_fp16) + begin;
     a.stride = rank_stride;
     a.w = master + begin;
-    a.m = m + begin;
-    a.v = v + begin;
+    a.m = m ? m + begin : nullptr;
+    a.v = v ? v + begin : nullptr;
     a.p = static_cast<__half*>(params_fp16) + begin;
     a.n = end - begin;
     a.P = P;
@@ -901,7 +935,7 @@ extern "C" int zero_adam_step_range(const void* grads_fp16, int64_t rank_stride,
     int rc = check_scalars(N, P, stage, t, lr, beta1, beta2, eps, mode);
     if (rc) return rc;
     if (rank_stride < N || begin < 0 || begin >= end || end > N) return ZERO_EINVAL;
-    if (!grads_fp16 || !master || !m || !v || !params_fp16) return ZERO_EINVAL;
+    if (!grads_fp16 || !master || !params_fp16) return ZERO_EINVAL; // m, v: checked by mode
     return launch_range(range_args(grads_fp16, rank_stride, begin, end, master, m, v, params_fp16, P), t, lr,
                         beta1, beta2, eps, mode, static_cast<cudaStream_t>(cuda_stream));
 }
@@ -915,7 +949,7 @@ extern "C" int zero_adam_step_bucketed(const void* grads_fp16, int64_t rank_stri
     int rc = check_scalars(N, P, stage, t, lr, beta1, beta2, eps, mode);
     if (rc) return rc;
     if (rank_stride < N || !buckets || n_buckets < 1) return ZERO_EINVAL;
-    if (!grads_fp16 || !master || !m || !v || !params_fp16) return ZERO_EINVAL;
+    if (!grads_fp16 || !master || !params_fp16) return ZERO_EINVAL; // m, v: checked by mode
     // every bucket in range and no two overlapping, before anything is enqueued
     std::vector<std::pair<int64_t, int64_t>> sorted;
     sorted.reserve(static_cast<size_t>(n_buckets));
@@ -929,7 +963,7 @@ extern "C" int zero_adam_step_bucketed(const void* grads_fp16, int64_t rank_stri
     // the buffers are validated once, for the whole vector
     StepArgs whole = range_args(grads_fp16, rank_stride, 0, N, master, m, v, params_fp16, P);
     int V = 1;
-    rc = prepare_range(whole, t, lr, beta1, beta2, eps, &V);
+    rc = prepare_range(whole, t, lr, beta1, beta2, eps, mode, &V);
     if (rc) return rc;
 
     cudaStream_t stream = static_cast<cudaStream_t>(step_stream);
@@ -1069,6 +1103,7 @@ extern "C" int zero_offload_step(const void* grads_fp16, int64_t rank_stride, fl
     int rc = check_scalars(N, P, stage, t, lr, beta1, beta2, eps, mode);
     if (rc) return rc;
     if (rank_stride < N || cpu_threads < 0 || cpu_threads > 1024) return ZERO_EINVAL;
+    if (mode > ZERO_MODE_FOLDED_STORAGE) return ZERO_EINVAL; // the host update is Adam
     if (!grads_fp16 || !master_host || !m_host || !v_host || !grad16_host || !params16_host || !params_fp16)
         return ZERO_EINVAL;
     if (reinterpret_cast<uintptr_t>(master_host) % 4 || reinterpret_cast<uintptr_t>(m_host) % 4 ||
@@ -1119,7 +1154,7 @@ extern "C" int zero_selftest_wait_timeout(const void* grads_fp16, int64_t rank_s
     a.n = N;
     a.P = P;
     int V = 1;
-    rc = prepare_range(a, t, lr, beta1, beta2, eps, &V);
+    rc = prepare_range(a, t, lr, beta1, beta2, eps, mode, &V);
     if (rc) return rc;
     const int sms = sm_count_of_current_device();
     if (sms <= 0) return record_cuda(cudaGetLastError());

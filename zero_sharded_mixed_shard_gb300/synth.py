@@ -60,6 +60,14 @@ def gpt2_small_numels(d: int = 768, layers: int = 12, vocab: int = 50257, ctx: i
     return [vocab * d, ctx * d] + block * layers + [d, d]
 
 
+def bytes_per_elem(P: int, mode: int) -> int:
+    """Bytes one step moves per element: P fp16 gradient reads, the fp32
+    state the optimizer reads and writes (master, m, v for Adam; master and
+    m with momentum; master for plain SGD), one fp16 parameter write."""
+    state = {3: 1, 4: 2}.get(mode, 3)
+    return 2 * P + 8 * state + 2
+
+
 def round_up(x: int, q: int) -> int:
     return -(-x // q) * q
 
