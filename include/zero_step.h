@@ -362,6 +362,36 @@ int zero_mlp4_zero3_step(const float* x, int32_t P, int32_t n, void* gathered_fp
                          float beta2, float eps, int32_t mode, int32_t pipelined,
                          void* main_stream, void* step_stream);
 
+/* zero_mlp4_zero3_step for callers that cannot allocate device memory (no
+ * counterpart in the pages).  Some host programs reserve all of a GPU's
+ * memory for their own allocator when they start and allow no allocation
+ * afterwards -- any buffer a library asked them for would have to come out
+ * of a budget they have already handed out -- and some services may not
+ * allocate once they are running.  Such a caller cannot provide the scratch
+ * zero_mlp4_zero3_step needs between its kernels (the all-gathered fp16
+ * parameters and every rank's fp16 gradients).  Here that scratch is a
+ * 256-byte array inside the library, fixed for the life of the process on
+ * every GPU that loads it; the caller passes only the inputs and outputs:
+ * x, master / m / v, the owners' fp16 shards and loss, as for
+ * zero_mlp4_zero3_step.
+ *  - Limit: the array holds at most 8 ranks' gradients; P outside [1, 8]
+ *    returns ZERO_EINVAL, as do the other bad arguments, before anything is
+ *    enqueued.
+ *  - Schedule: the serial one (pipelined = 0) on cuda_stream; the call
+ *    neither allocates nor creates events.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *    that first call before any stream capture.
+ *  - Every call on a device uses the same array, which keeps the contents
+ *    of the last call (each call writes every entry before reading it, so
+ *    nothing needs clearing).  Calls whose work overlaps on the GPU -- on
+ *    two streams, or from two host threads -- race on it: order them.
+ * Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
+int zero_mlp4_zero3_step_noalloc(const float* x, int32_t P, int32_t n, float* master, float* m,
+                                 float* v, void* shard_fp16, float* loss, int64_t t, float lr,
+                                 float beta1, float beta2, float eps, int32_t mode,
+                                 void* cuda_stream);
+
 /* Bounded waits that gave up, over every step launched on the current
  * device since the last reset.  The fused kernels wait on shared-memory
  * barriers for their own bulk copies; each wait gives up after 2 seconds,

@@ -35,7 +35,7 @@ EXPORTED = ("zero_init_layout", "zero_free_layout", "zero_shard_range", "zero_me
             "zero_adam_step", "zero_adam_step_shard", "zero_plan_buckets", "zero_adam_step_range",
             "zero_adam_step_bucketed", "zero_reduce_scatter_fp16", "zero_cpu_adam",
             "zero_offload_step", "zero_mlp4_loss", "zero_mlp4_layer_grads",
-            "zero_mlp4_zero3_step", "zero_device_timeouts",
+            "zero_mlp4_zero3_step", "zero_mlp4_zero3_step_noalloc", "zero_device_timeouts",
             "zero_selftest_wait_timeout", "zero_strerror",
             "zero_last_cuda_error", "zero_last_cuda_error_string")
 
@@ -128,6 +128,9 @@ def lib() -> ctypes.CDLL:
     L.zero_mlp4_zero3_step.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, i64,
                                        f32, f32, f32, f32, i32, i32, vp, vp]
     L.zero_mlp4_zero3_step.restype = ctypes.c_int
+    L.zero_mlp4_zero3_step_noalloc.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i64, f32, f32,
+                                               f32, f32, i32, vp]
+    L.zero_mlp4_zero3_step_noalloc.restype = ctypes.c_int
     L.zero_selftest_wait_timeout.argtypes = [vp, i64, vp, vp, vp, vp, i64, i32, i32, i64,
                                              f32, f32, f32, f32, i32, vp]
     L.zero_selftest_wait_timeout.restype = ctypes.c_int
@@ -371,3 +374,16 @@ def zero_mlp4_zero3_step(x, P: int, n: int, gathered16, master, m, v, shard16, g
                                     _stream(step_stream) if step_stream is not None else None)
     if rc:
         raise ZeroError(rc, "zero_mlp4_zero3_step")
+
+
+def zero_mlp4_zero3_step_noalloc(x, P: int, n: int, master, m, v, shard16, loss, t: int,
+                                 lr: float, beta1: float, beta2: float, eps: float, mode: int,
+                                 stream=None) -> None:
+    """The ZeRO-3 MLP step for callers that cannot allocate device memory:
+    its scratch lives inside the library (at most 8 ranks; calls that
+    overlap on the GPU race on it; see include/zero_step.h)."""
+    rc = lib().zero_mlp4_zero3_step_noalloc(_addr(x), P, n, _addr(master), _addr(m), _addr(v),
+                                            _addr(shard16), _addr(loss), t, lr, beta1, beta2, eps,
+                                            mode, _stream(stream))
+    if rc:
+        raise ZeroError(rc, "zero_mlp4_zero3_step_noalloc")

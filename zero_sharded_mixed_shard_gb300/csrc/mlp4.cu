@@ -24,6 +24,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <cmath>
 #include <cstdint>
 
 #include "zero_step.h"
@@ -221,5 +223,85 @@ extern "C" int zero_mlp4_zero3_step(const float* x, int32_t P, int32_t n, void* 
         if ((e = cudaStreamWaitEvent(ms, step_done, 0)) != cudaSuccess) return fail(e);
     }
     cleanup();
+    return ZERO_OK;
+}
+
+// ---------------------------------------------------------------------------
+// A variant of zero_mlp4_zero3_step for callers that cannot allocate device
+// memory: its scratch -- the all-gathered fp16 parameters and every rank's
+// fp16 gradients -- lives in one file-scope device array instead of buffers
+// the caller provides.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// Scratch layout (fp16): [0, 8) the all-gathered parameters, then 8 ranks x
+// 8 gradients at rank stride 8.  144 bytes used, 256 reserved.
+constexpr int kScratchHalves = 128;
+constexpr int kScratchGrads = kParams;          // offset of rank 0's gradients
+constexpr int kScratchRankStride = kParams;
+static_assert(kScratchGrads + kMaxRanks * kScratchRankStride <= kScratchHalves, "scratch too small");
+
+static __device__ __align__(256) __half g_mlp4_scratch[kScratchHalves];
+
+// Device address of g_mlp4_scratch, looked up once per device with that
+// device current.  Host code may not use the symbol's name as an address.
+std::atomic<void*> g_scratch_addr[64];
+
+int scratch_address(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return zero_record_cuda_error(static_cast<int>(e));
+    if (dev < 0 || dev >= 64) return ZERO_EINVAL;
+    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        e = cudaGetSymbolAddress(&p, g_mlp4_scratch);
+        if (e != cudaSuccess) return zero_record_cuda_error(static_cast<int>(e));
+        g_scratch_addr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return ZERO_OK;
+}
+
+} // namespace
+
+extern "C" int zero_mlp4_zero3_step_noalloc(const float* x, int32_t P, int32_t n, float* master, float* m,
+                                            float* v, void* shard_fp16, float* loss, int64_t t, float lr,
+                                            float beta1, float beta2, float eps, int32_t mode, void* cuda_stream)
+{
+    // the scratch holds at most kMaxRanks ranks' gradients
+    if (P < 1 || P > kMaxRanks) return ZERO_EINVAL;
+    if (!x || !master || !m || !v || !shard_fp16 || !loss || n < 1 || t < 1) return ZERO_EINVAL;
+    if (mode < 0 || mode > ZERO_MODE_MOMENTUM || !isfinite(lr) || !isfinite(beta1) || !isfinite(beta2) ||
+        !isfinite(eps) || !(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f) || !(eps >= 0.0f))
+        return ZERO_EINVAL; // refused before anything is enqueued
+    void* scratch = nullptr;
+    int rc = scratch_address(&scratch);
+    if (rc) return rc;
+    __half* gathered = static_cast<__half*>(scratch);
+    __half* grads = gathered + kScratchGrads;
+    // the serial schedule of zero_mlp4_zero3_step on one stream: it creates
+    // no events and allocates nothing; every scratch entry read below is
+    // written earlier in the same call, so nothing has to be cleared
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    const cudaError_t e = cudaMemcpyAsync(gathered, shard_fp16, kParams * sizeof(__half), cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return zero_record_cuda_error(static_cast<int>(e));
+    rc = zero_mlp4_loss(gathered, x, P, n, loss, st);
+    if (rc) return rc;
+    const int64_t M = (kParams + P - 1) / P;
+    __half* shards = static_cast<__half*>(shard_fp16);
+    for (int layer = 4; layer >= 1; --layer) {
+        rc = zero_mlp4_layer_grads(layer, gathered, x, P, n, grads, kScratchRankStride, st);
+        if (rc) return rc;
+        for (int32_t k = P - 1; k >= 0; --k) {
+            const int64_t b = k * M < kParams ? k * M : kParams;
+            const int64_t end = b + M < kParams ? b + M : kParams;
+            if (b >= end || static_cast<int>(b / 2) + 1 != layer) continue; // shard k's lowest layer
+            rc = zero_adam_step_shard(grads, kScratchRankStride, b, k, master + b, m + b, v + b, shards + b,
+                                      kParams, P, 3, t, lr, beta1, beta2, eps, mode, st);
+            if (rc) return rc;
+        }
+    }
     return ZERO_OK;
 }
