@@ -410,37 +410,71 @@ def run_ours(args, wl, mode, dist):
 
 def run_e2e(z, wl, mode, g, master, m, v, params, stride, stream, device, dist, t, K_e2e):
     """Each step: pinned host gradients -> device, the step, gathered fp16
-    parameters -> pinned host; all inside the timed region."""
+    parameters -> pinned host; all inside the timed region.
+
+    Steps are pipelined the way a training loop would: the upload of step
+    k+1's gradients (into the second of two device buffers, on its own
+    stream) runs while step k's kernel and the download of its parameters
+    run; step k+1's kernel waits for its upload and for the download of
+    step k's parameters (which it overwrites)."""
     import torch
     host_g = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
     host_g.copy_(g)
     host_p = torch.empty(params.shape, dtype=params.dtype, pin_memory=True)
-    dev_g = g
+    dev_g = [g, torch.empty_like(g)]
+    up = torch.cuda.Stream(device)
+    down = torch.cuda.Stream(device)
     for _ in range(2):   # warm the copy engines
-        dev_g.copy_(host_g, non_blocking=True)
+        dev_g[1].copy_(host_g, non_blocking=True)
         host_p.copy_(params, non_blocking=True)
     torch.cuda.synchronize()
     dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(K_e2e):
+    up.wait_stream(stream)
+    down.wait_stream(stream)
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    downloaded = torch.cuda.Event()
+    for k in range(2):
+        consumed[k].record(stream)
+    downloaded.record(down)
+    # upload of step 0
+    with torch.cuda.stream(up):
+        dev_g[0].copy_(host_g, non_blocking=True)
+        uploaded[0].record(up)
+    for k in range(K_e2e):
+        b = k % 2
+        if k + 1 < K_e2e:        # the next step's upload, into the other buffer
+            nb = (k + 1) % 2
+            up.wait_event(consumed[nb])
+            with torch.cuda.stream(up):
+                dev_g[nb].copy_(host_g, non_blocking=True)
+                uploaded[nb].record(up)
+        stream.wait_event(uploaded[b])
+        stream.wait_event(downloaded)        # the previous parameters have left
         t += 1
-        dev_g.copy_(host_g, non_blocking=True)
         if wl.shard is None:
-            z.zero_adam_step(dev_g, stride, master, m, v, params, wl.N, wl.P, wl.stage, t, wl.lr,
-                             wl.b1, wl.b2, wl.eps, mode, stream)
+            z.zero_adam_step(dev_g[b], stride, master, m, v, params, wl.N, wl.P, wl.stage, t,
+                             wl.lr, wl.b1, wl.b2, wl.eps, mode, stream)
         else:
-            z.zero_adam_step_shard(dev_g, stride, 0, wl.shard, master, m, v, params, wl.N, wl.P,
-                                   wl.stage, t, wl.lr, wl.b1, wl.b2, wl.eps, mode, stream)
-        host_p.copy_(params, non_blocking=True)
+            z.zero_adam_step_shard(dev_g[b], stride, 0, wl.shard, master, m, v, params, wl.N,
+                                   wl.P, wl.stage, t, wl.lr, wl.b1, wl.b2, wl.eps, mode, stream)
+        consumed[b].record(stream)
+        down.wait_event(consumed[b])
+        with torch.cuda.stream(down):
+            host_p.copy_(params, non_blocking=True)
+            downloaded.record(down)
+    stream.wait_event(downloaded)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = dist.max(e0.elapsed_time(e1), device)
     return {"value": wl.elems * K_e2e * dist.world / (ms / 1e3), "unit": "params/s",
             "h2d_bytes_per_step": host_g.numel() * host_g.element_size(),
             "d2h_bytes_per_step": host_p.numel() * host_p.element_size(),
-            "steps": K_e2e, "ms_per_step": ms / K_e2e}
+            "steps": K_e2e, "ms_per_step": ms / K_e2e,
+            "pipelining": "upload of step k+1 overlaps step k's kernel and download"}
 
 
 def run_overlap(args, wl, mode, dist):
