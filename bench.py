@@ -64,6 +64,11 @@ def parse_args(argv=None):
                     help="inner dimension of the synthetic backward's GEMMs")
     ap.add_argument("--step-priority", choices=("high", "normal"), default="high",
                     help="priority of the step's stream in the overlap leg")
+    ap.add_argument("--step-sms", type=int, default=0,
+                    help="overlap leg: SMs the step of every bucket but the last may occupy "
+                         "(0 = all); the last bucket, which nothing hides, runs uncapped")
+    ap.add_argument("--gemm-carveout", type=int, default=0,
+                    help="overlap leg: SMs the backward's cuBLAS GEMMs leave free")
     ap.add_argument("--offload", action="store_true",
                     help="time the ZeRO-Offload step (update on the host CPU) instead")
     ap.add_argument("--mlp4", action="store_true",
@@ -516,6 +521,14 @@ def run_overlap(args, wl, mode, dist):
     step_stream = torch.cuda.Stream(dev, priority=-1 if args.step_priority == "high" else 0)
     t_counter = [0]
 
+    carve = args.gemm_carveout
+    if carve and not hasattr(torch._C, "_set_sm_carveout_experimental"):
+        raise SystemExit("--gemm-carveout needs torch._C._set_sm_carveout_experimental")
+
+    def set_carveout(n):
+        if carve:
+            torch._C._set_sm_carveout_experimental(n if n else None)
+
     def backward(stream, events=None):
         with torch.cuda.stream(stream):
             for i, (b, e, _, _) in enumerate(buckets):
@@ -532,8 +545,18 @@ def run_overlap(args, wl, mode, dist):
 
     def step_bucketed(stream, events):
         t_counter[0] += 1
-        z.zero_adam_step_bucketed(g, stride, *state, N, P, wl.stage, t_counter[0], wl.lr, wl.b1,
-                                  wl.b2, wl.eps, mode, buckets, ready_events=events, stream=stream)
+        args_ = (g, stride, *state, N, P, wl.stage, t_counter[0], wl.lr, wl.b1, wl.b2, wl.eps, mode)
+        if args.step_sms and len(buckets) > 1:
+            prev = z.zero_set_step_max_sms(args.step_sms)
+            try:
+                z.zero_adam_step_bucketed(*args_, buckets[:-1], ready_events=events[:-1],
+                                          stream=stream)
+            finally:
+                z.zero_set_step_max_sms(prev)
+            z.zero_adam_step_bucketed(*args_, buckets[-1:], ready_events=events[-1:],
+                                      stream=stream)
+        else:
+            z.zero_adam_step_bucketed(*args_, buckets, ready_events=events, stream=stream)
 
     def timed(fn, reps):
         for _ in range(args.warmup):
@@ -561,6 +584,12 @@ def run_overlap(args, wl, mode, dist):
         join(step_stream, prod_stream)
         backward(prod_stream)
 
+    def only_backward_carved():
+        join(step_stream, prod_stream)
+        set_carveout(carve)
+        backward(prod_stream)
+        set_carveout(0)
+
     def only_step():
         join(prod_stream, step_stream)
         step_whole(step_stream)
@@ -573,13 +602,16 @@ def run_overlap(args, wl, mode, dist):
     def overlapped():
         join(step_stream, prod_stream)
         events = [torch.cuda.Event() for _ in buckets]
+        set_carveout(carve)
         backward(prod_stream, events)
+        set_carveout(0)
         step_bucketed(step_stream, events)
 
     t_b = timed(only_backward, reps)
     t_s = timed(only_step, reps)
     t_serial = timed(serial, reps)
     t_over = timed(overlapped, reps)
+    t_b_carved = timed(only_backward_carved, reps) if carve else t_b
     hidden = (t_serial - t_over) / t_s
     if dist.rank == 0:
         line = {
@@ -590,8 +622,10 @@ def run_overlap(args, wl, mode, dist):
                                                 buckets=len(buckets), bucket_elems=args.bucket_elems,
                                                 backward="one fp16 GEMM [L/768,k]x[k,768] per bucket "
                                                          f"per rank, k={k}",
-                                                step_stream_priority=args.step_priority),
-            "backward_ms": t_b, "step_ms": t_s, "serial_ms": t_serial, "overlapped_ms": t_over,
+                                                step_stream_priority=args.step_priority,
+                                                step_sms=args.step_sms or "all",
+                                                gemm_carveout_sms=carve),
+            "backward_ms": t_b, "backward_carved_ms": t_b_carved, "step_ms": t_s, "serial_ms": t_serial, "overlapped_ms": t_over,
             "gpu_launches_per_rep": len(buckets) * (P + 1),
         }
         print(json.dumps(line), flush=True)

@@ -263,6 +263,22 @@ int zero_adam_step_bucketed(const void* grads_fp16, int64_t rank_stride, float* 
                             const zero_bucket_t* buckets, int32_t n_buckets,
                             void* const* ready_events, void* step_stream);
 
+/* How many SMs a fused step may occupy (no counterpart on the pages; the
+ * counterpart of cuBLAS's SM-count target).  [P3] §1.6.7 runs communication
+ * and computation on separate CUDA streams at the same time; on one GPU they
+ * can only run side by side when each leaves SMs to the other.  A step
+ * enqueued while max_sms > 0 launches at most max_sms SMs' worth of CTAs
+ * (the bulk-copy kernel: max_sms CTAs of one per SM), so a producer kernel
+ * held below (SM count - max_sms) SMs keeps the rest; 0 (the default) = every
+ * SM; a value above the SM count acts as 0.  Process-wide, read when a step
+ * is enqueued (zero_adam_step, _shard, _range, each bucket of _bucketed, the
+ * ZeRO-3 example's steps), so a caller can enqueue some buckets capped and
+ * the rest uncapped.  The results do not depend on it: tiles are dealt to the
+ * CTAs in a fixed round-robin order and each element's arithmetic is the
+ * same.  *previous (if not NULL) receives the value it replaces.  Host only,
+ * thread-safe (atomic).  Errors: ZERO_EINVAL (max_sms < 0). */
+int zero_set_step_max_sms(int32_t max_sms, int32_t* previous);
+
 /* ------------------------------------------------------------------------ */
 /* ZeRO-Offload ([P3] §2.2 Offload 策略: the data-flow graph is cut along    */
 /* the fp16 gradient and fp16 parameter edges, so the parameter update and   */

@@ -153,3 +153,17 @@ def test_unused_state_may_be_null_but_used_state_may_not(zlib):
     # first failing check is then on a used one
     assert _call(zlib, mode=3, m=W + 1, v=W, params=PP + 1) == zlib.ZERO_EALIGN
     assert _call(zlib, mode=4, v=MM + 1, m=W + 8) == zlib.ZERO_EOVERLAP
+
+
+def test_step_max_sms_setting(zlib):
+    """Host-only: the cap is stored, returned as the previous value, and a
+    negative cap is refused without changing it."""
+    prev = zlib.zero_set_step_max_sms(12)
+    try:
+        assert zlib.zero_set_step_max_sms(0) == 12
+        with pytest.raises(zlib.ZeroError) as e:
+            zlib.zero_set_step_max_sms(-1)
+        assert e.value.code == zlib.ZERO_EINVAL
+        assert zlib.zero_set_step_max_sms(0) == 0
+    finally:
+        zlib.zero_set_step_max_sms(prev)

@@ -425,3 +425,29 @@ def test_sgd_and_momentum_match_oracle(z, mode, big):
     assert bool((sentinel == 1234.5).all())
     if mode == 3:
         assert np.array_equal(host_state(s)[1], m0)        # m untouched by plain SGD
+
+
+# ---------------------------------------------------------------------------
+# the SM cap (zero_set_step_max_sms): fewer CTAs, the same bytes
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cap", [1, 5, 76, 1000])
+def test_step_max_sms_leaves_results_unchanged(z, cap):
+    """A capped step deals the same tiles to fewer CTAs: both kernels (a
+    bulk-pipeline problem with a partial tile and a ragged tail, and a small
+    vector-path one) must still agree with the oracle bit for bit."""
+    prev = z.zero_set_step_max_sms(cap)
+    try:
+        for P, N in ((8, _tma_size(4101)), (5, 70_001)):
+            stride = synth.round_up(N, 8)
+            w0, m0, v0, p0 = synth.np_state(N, 60 + cap)
+            ref = [w0.copy(), m0.copy(), v0.copy()]
+            s = dev_state(w0, m0, v0, p0)
+            for t in (1, 2):
+                codes = synth.np_grads(P, N, stride, 1e-3, 900 + t + cap, heavy_tail_frac=0.01)
+                gpu_step(z, dev_u16(codes), stride, s, N, P, t, 0)
+                p_ref = oracle.adam_elems(codes, stride, P, *ref, t, LR, B1, B2, EPS, 0, threads=8)
+                assert max_ulps(host_state(s), ref + [p_ref]) == (0, 0), f"cap={cap} P={P} t={t}"
+    finally:
+        assert z.zero_set_step_max_sms(prev) == cap
+    assert z.zero_device_timeouts() == 0

@@ -33,7 +33,7 @@ MODE_MOMENTUM = 4
 # every symbol include/zero_step.h declares
 EXPORTED = ("zero_init_layout", "zero_free_layout", "zero_shard_range", "zero_memory_bytes",
             "zero_adam_step", "zero_adam_step_shard", "zero_plan_buckets", "zero_adam_step_range",
-            "zero_adam_step_bucketed", "zero_reduce_scatter_fp16", "zero_cpu_adam",
+            "zero_adam_step_bucketed", "zero_set_step_max_sms", "zero_reduce_scatter_fp16", "zero_cpu_adam",
             "zero_offload_step", "zero_mlp4_loss", "zero_mlp4_layer_grads",
             "zero_mlp4_zero3_step", "zero_mlp4_zero3_step_noalloc", "zero_device_timeouts",
             "zero_selftest_wait_timeout", "zero_strerror",
@@ -114,6 +114,8 @@ def lib() -> ctypes.CDLL:
                                           f32, f32, f32, f32, i32, ctypes.POINTER(zero_bucket_t),
                                           i32, ctypes.POINTER(ctypes.c_void_p), vp]
     L.zero_adam_step_bucketed.restype = ctypes.c_int
+    L.zero_set_step_max_sms.argtypes = [i32, ctypes.POINTER(ctypes.c_int32)]
+    L.zero_set_step_max_sms.restype = ctypes.c_int
     L.zero_reduce_scatter_fp16.argtypes = [vp, i64, i64, i32, i64, vp, vp]
     L.zero_reduce_scatter_fp16.restype = ctypes.c_int
     L.zero_cpu_adam.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, f32, f32, f32, i32, i32]
@@ -239,6 +241,15 @@ def zero_adam_step_shard(grads, rank_stride: int, grad_offset: int, k: int, mast
                                     lr, beta1, beta2, eps, mode, _stream(stream))
     if rc:
         raise ZeroError(rc, "zero_adam_step_shard")
+
+
+def zero_set_step_max_sms(max_sms: int) -> int:
+    """Cap the SMs a fused step occupies (0 = all); returns the previous cap."""
+    prev = ctypes.c_int32()
+    rc = lib().zero_set_step_max_sms(max_sms, ctypes.byref(prev))
+    if rc:
+        raise ZeroError(rc, "zero_set_step_max_sms")
+    return prev.value
 
 
 def zero_device_timeouts(reset: bool = False) -> int:

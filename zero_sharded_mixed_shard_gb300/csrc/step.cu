@@ -843,20 +843,34 @@ int launch_vector(const StepArgs& a, int V, int mode, int sms, cudaStream_t stre
 // the vector path, whose many CTAs start and finish sooner.
 constexpr int kMinTilesPerSm = 4;
 
+// The SMs a fused step may occupy (0 = all of them); read when a step is
+// enqueued.  Below the SM count it leaves SMs free for work on other streams.
+std::atomic<int> g_step_max_sms{0};
+
 int launch_range(StepArgs a, int64_t t, float lr, float b1, float b2, float eps, int mode,
                  cudaStream_t stream)
 {
     int V = 1;
     int rc = prepare_range(a, t, lr, b1, b2, eps, mode, &V);
     if (rc) return rc;
-    const int sms = sm_count_of_current_device();
+    int sms = sm_count_of_current_device();
     if (sms <= 0) return record_cuda(cudaGetLastError());
+    const int cap = g_step_max_sms.load(std::memory_order_relaxed);
+    if (cap > 0 && cap < sms) sms = cap;
     if (V == 8 && bulk_tiles(a) >= static_cast<long long>(kMinTilesPerSm) * sms)
         return launch_tma(a, mode, sms, stream);
     return launch_vector(a, V, mode, sms, stream);
 }
 
 } // namespace
+
+extern "C" int zero_set_step_max_sms(int32_t max_sms, int32_t* previous)
+{
+    if (max_sms < 0) return ZERO_EINVAL;
+    const int old = g_step_max_sms.exchange(max_sms, std::memory_order_relaxed);
+    if (previous) *previous = old;
+    return ZERO_OK;
+}
 
 extern "C" int zero_adam_step(const void* grads_fp16, int64_t rank_stride, float* master, float* m,
                               float* v, void* params_fp16, int64_t N, int32_t P, int32_t stage,
