@@ -635,9 +635,9 @@ def run_overlap(args, wl, mode, dist):
 
 def run_offload(args, wl, mode, dist):
     """ZeRO-Offload step: fp16 gradient mean to page-locked host memory, CPU
-    Adam per shard in stream order, fp16 weights back into the device
-    vector.  Also timed alone: the GPU reduce (its host writes) and the host
-    Adam on all host cores."""
+    Adam per piece of shards as its gradients arrive, fp16 weights back into
+    the device vector while the next piece is updated.  Also timed alone:
+    the GPU reduce (its host writes) and the host Adam on all host cores."""
     import torch
 
     import zero_sharded_mixed_shard_gb300 as z
@@ -652,7 +652,7 @@ def run_offload(args, wl, mode, dist):
     dev = torch.device("cuda", dist.local_rank)
     P, N = wl.P, wl.N
     stride = wl.rank_stride(True)
-    cores = os.cpu_count() or 1
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     g = synth.torch_grads(P, N, stride, wl.grad_sigma, wl.seed, dev, wl.heavy_tail_frac,
                           wl.zero_frac, step=1)
     dstate = synth.torch_state(N, wl.seed, dev, wl.master_sigma)
@@ -668,7 +668,7 @@ def run_offload(args, wl, mode, dist):
     def step():
         t[0] += 1
         z.zero_offload_step(g, stride, *host, g16_h, p16_h, params, N, P, wl.stage, t[0], wl.lr,
-                            wl.b1, wl.b2, wl.eps, mode, cores, stream)
+                            wl.b1, wl.b2, wl.eps, mode, 0, stream)
 
     def reduce_only():
         z.zero_reduce_scatter_fp16(g, stride, 0, P, N, g16_h, stream)
@@ -692,8 +692,7 @@ def run_offload(args, wl, mode, dist):
     # the host update alone, all cores, same buffers
     t0 = time.perf_counter()
     for k in range(reps):
-        z.zero_cpu_adam(g16_h, *host, p16_h, N, t[0] + k + 1, wl.lr, wl.b1, wl.b2, wl.eps, mode,
-                        cores)
+        z.zero_cpu_adam(g16_h, *host, p16_h, N, t[0] + k + 1, wl.lr, wl.b1, wl.b2, wl.eps, mode, 0)
     ms_cpu = (time.perf_counter() - t0) * 1e3 / reps
     if dist.rank == 0:
         line = {

@@ -304,32 +304,43 @@ int zero_reduce_scatter_fp16(const void* grads_fp16, int64_t rank_stride, int64_
  * fp32 master / m / v from the fp16 gradient grad_fp16, and the fp16 cast of
  * the new weights into params_fp16 -- the same operations, in the same order
  * and precision, as zero_adam_step (given the gradient).  `threads` host
- * threads take chunks of 16 Ki elements as they are free (0 = one per
- * hardware thread; the calling thread is one of them).  Runs synchronously
- * on the calling thread.
+ * threads take chunks of 16 Ki elements as they are free (0 = one per CPU
+ * in the process's affinity mask, which is also the most used; the calling
+ * thread is one of them, the others come from a pool created on the first
+ * call and kept for the life of the process).  One call runs at a time:
+ * concurrent calls wait for each other.  Runs synchronously on the calling
+ * thread.
  * Errors: ZERO_EINVAL (null pointer with n > 0, n < 0, t < 1, bad mode or
  * hyper-parameter, threads outside [0, 1024]). */
 int zero_cpu_adam(const void* grad_fp16, float* master, float* m, float* v, void* params_fp16,
                   int64_t n, int64_t t, float lr, float beta1, float beta2, float eps,
                   int32_t mode, int32_t threads);
 
-/* One ZeRO-Offload step of the whole vector, enqueued on cuda_stream:
- *   1. zero_reduce_scatter_fp16 of all N elements into grad16_host;
- *   2. one host function (cudaLaunchHostFunc) that runs zero_cpu_adam over
- *      every shard k = 0..P-1 ([min(kM,N), min((k+1)M,N)), contiguous, so
- *      one pass over [0, N)) with cpu_threads host threads (0 = all
- *      hardware threads) taking chunks as they are free, writing
- *      params16_host;
- *   3. one async copy per shard of its fp16 weights into params_fp16 at
- *      offset kM (the all-gather's output).
+/* One ZeRO-Offload step of the whole vector.  The shards k = 0..P-1
+ * ([min(kM,N), min((k+1)M,N))) are grouped into at most 16 pieces of whole
+ * shards (fewer when N is small: at least 2^20 elements a piece), and for
+ * each piece, in order:
+ *   1. zero_reduce_scatter_fp16 of the piece into grad16_host, on
+ *      cuda_stream;
+ *   2. a host function (cudaLaunchHostFunc) that runs zero_cpu_adam on the
+ *      piece with cpu_threads host threads (0 = all), writing params16_host,
+ *      on an internal stream that waits for step 1 of the piece;
+ *   3. one async copy per shard of the piece of its fp16 weights into
+ *      params_fp16 at offset kM (the all-gather's output), on a second
+ *      internal stream that waits for step 2 of the piece.
+ * So the GPU reduces piece j+1 and piece j-1's weights cross back while the
+ * host updates piece j.  cuda_stream then waits for both internal streams
+ * (one pair per device, created on the first call and kept), so everything
+ * after the call on cuda_stream sees the whole step, as if it had run in
+ * stream order.  The results do not depend on the pieces.
  * grads_fp16 and params_fp16 are device memory; master_host, m_host, v_host
  * (fp32 [N]) and grad16_host, params16_host (fp16 [N]) are page-locked host
  * memory that the caller keeps alive, and leaves alone, until the stream has
  * passed this step.  The call returns at once.  Numerically the step differs
  * from zero_adam_step only in that the gradient mean is rounded to fp16 on
  * its way to the host.  Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ENOMEM (host
- * bookkeeping), ZERO_ECUDA (work enqueued before the refused call stays
- * enqueued). */
+ * bookkeeping), ZERO_ECUDA (pieces enqueued before the failure stay
+ * enqueued, and cuda_stream still waits for them when that is possible). */
 int zero_offload_step(const void* grads_fp16, int64_t rank_stride, float* master_host, float* m_host,
                       float* v_host, void* grad16_host, void* params16_host, void* params_fp16,
                       int64_t N, int32_t P, int32_t stage, int64_t t, float lr, float beta1,

@@ -84,3 +84,49 @@ def test_cpu_adam_rejects(zlib):
     with pytest.raises(zlib.ZeroError):
         zlib.zero_cpu_adam(None, a, a, a, h, 4, 1, LR, B1, B2, EPS, 0, 1)
     zlib.zero_cpu_adam(None, None, None, None, None, 0, 1, LR, B1, B2, EPS, 0, 1)  # n = 0
+
+
+def test_cpu_adam_concurrent_callers_share_the_pool(zlib, oracle_mod):
+    """The host threads are a pool kept between calls; calls from several
+    threads at once queue on it and each still matches the oracle bit for
+    bit (ctypes releases the GIL for the duration of each call)."""
+    import threading
+
+    n, P = 200_003, 4
+    cases = []
+    for k in range(6):
+        w, m, v, _ = synth.np_state(n, 50 + k)
+        codes = synth.np_grads(P, n, n, 1e-3, 60 + k)
+        ref = [w.copy(), m.copy(), v.copy()]
+        p_ref, g16 = oracle_mod.offload_elems(codes, n, P, *ref, 2, LR, B1, B2, EPS, k % 3)
+        cases.append((w, m, v, np.empty(n, np.uint16), g16, ref, p_ref, k % 3, (0, 1, 2, 5)[k % 4]))
+    errors = []
+
+    def run(case):
+        w, m, v, p, g16, _, _, mode, threads = case
+        try:
+            for _ in range(3):   # same inputs each time: the last call's bytes are checked
+                w2, m2, v2 = w.copy(), m.copy(), v.copy()
+                zlib.zero_cpu_adam(g16, w2, m2, v2, p, n, 2, LR, B1, B2, EPS, mode, threads)
+            w[:], m[:], v[:] = w2, m2, v2
+        except Exception as e:   # pragma: no cover - reported below
+            errors.append(e)
+
+    ths = [threading.Thread(target=run, args=(c,)) for c in cases]
+    for th in ths:
+        th.start()
+    for th in ths:
+        th.join()
+    assert not errors
+    for w, m, v, p, _, ref, p_ref, mode, threads in cases:
+        for got, exp in zip((w, m, v), ref):
+            assert _same32(got, exp), (mode, threads)
+        assert _same16(p, p_ref), (mode, threads)
+
+
+def test_cpu_adam_more_threads_than_cpus(zlib, oracle_mod):
+    """A thread count above the CPUs available is capped, not an error."""
+    n, P = 100_000, 2
+    w, m, v, _ = synth.np_state(n, 77)
+    codes = synth.np_grads(P, n, n, 1e-3, 78)
+    _check(zlib, oracle_mod, codes, n, P, w, m, v, 1, 0, 1024)

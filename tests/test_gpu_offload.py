@@ -1,7 +1,8 @@
 """ZeRO-Offload on the GPU machine (ZeRO 技术原理：进阶与 Offload §2.2, §2.3): the
 GPU reduces the ranks' gradients and sends the fp16 mean to page-locked host
-memory; host functions run the CPU Adam of each shard in stream order; the
-fp16 weights are copied back into the gathered device vector.  Checked
+memory; host functions run the CPU Adam of each piece (a group of shards)
+as its gradients arrive; the fp16 weights are copied back into the gathered
+device vector while the next piece is updated.  Checked
 against the oracle's offload step bit for bit."""
 import numpy as np
 import pytest
@@ -47,9 +48,12 @@ def test_reduce_to_fp16_mean(z, P, N, stride, off):
     assert np.array_equal(out_host.view(torch.int16).numpy().view(np.uint16), g16_ref)
 
 
-@pytest.mark.parametrize("P,mode", [(4, 0), (8, 1), (13, 2)])
-def test_offload_step_matches_oracle(z, P, mode):
-    N = 1_000_003
+@pytest.mark.parametrize("P,N,mode", [(4, 1_000_003, 0), (8, 1_000_003, 1), (13, 1_000_003, 2),
+                                      (8, 6_000_011, 0), (33, 9_000_007, 2)])
+def test_offload_step_matches_oracle(z, P, N, mode):
+    """One piece (N below 2^20 per piece) and pipelines of several pieces:
+    6 pieces of uneven shard groups (P = 8), 9 pieces of 3-4 shards each
+    with a short last shard (P = 33)."""
     stride = synth.round_up(N, 8)
     w0, m0, v0, p0 = synth.np_state(N, 20 + P)
     master, m, v = (_pinned(N, torch.float32) for _ in range(3))

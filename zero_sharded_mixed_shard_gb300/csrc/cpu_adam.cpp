@@ -23,10 +23,18 @@
 // passes: widen the fp16 gradient into a float buffer, the fp32 Adam loop
 // (only float loads and stores, branch-free, so it vectorises), narrow the
 // new weights to fp16.
+//
+// The threads are a pool created on the first call and kept for the life of
+// the process, so a call (and each piece of a pipelined offload step) pays
+// no thread creation.
+#include <sched.h>
+
 #include <atomic>
 #include <cmath>
+#include <condition_variable>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <thread>
 #include <vector>
 
@@ -98,6 +106,98 @@ void adam_chunk(int mode, const uint16_t* g16, float* w, float* m, float* v, uin
     for (int64_t i = 0; i < n; ++i) p16[i] = narrow(w[i]);
 }
 
+// Worker threads that sleep on a condition variable between jobs.  One job
+// runs at a time (concurrent callers queue on job_mu_); the caller works on
+// it too and returns once every helper has finished, so the job's data may
+// live on the caller's stack.  The pool is never destroyed: its threads are
+// parked in a wait when the process exits.
+class HostPool {
+public:
+    static HostPool& get()
+    {
+        static HostPool* pool = new HostPool(); // leaked on purpose (see above)
+        return *pool;
+    }
+
+    int size() const { return static_cast<int>(threads_.size()); }
+
+    // body(ctx) on the calling thread and on `helpers` pool threads.
+    void run(int helpers, void (*body)(void*), void* ctx)
+    {
+        std::lock_guard<std::mutex> job(job_mu_);
+        if (helpers > size()) helpers = size();
+        {
+            std::lock_guard<std::mutex> lk(mu_);
+            body_ = body;
+            ctx_ = ctx;
+            want_ = helpers;
+            pending_ = helpers;
+            ++gen_;
+        }
+        if (helpers > 0) cv_.notify_all();
+        body(ctx);
+        std::unique_lock<std::mutex> lk(mu_);
+        done_cv_.wait(lk, [&] { return pending_ == 0; });
+    }
+
+private:
+    // One thread per CPU this process may run on (its affinity mask, which a
+    // container may set below the machine's count), the caller included.
+    static int usable_cpus()
+    {
+        cpu_set_t set;
+        if (sched_getaffinity(0, sizeof(set), &set) == 0) {
+            const int n = CPU_COUNT(&set);
+            if (n > 0) return n;
+        }
+        const int hc = static_cast<int>(std::thread::hardware_concurrency());
+        return hc > 0 ? hc : 1;
+    }
+
+    HostPool()
+    {
+        int n = usable_cpus() - 1;
+        if (n > 1023) n = 1023;
+        for (int i = 0; i < n; ++i) {
+            try {
+                threads_.emplace_back(&HostPool::worker, this, i);
+            } catch (...) {
+                break; // fewer helpers: every job still completes
+            }
+        }
+    }
+
+    void worker(int idx)
+    {
+        uint64_t seen = 0;
+        for (;;) {
+            void (*body)(void*) = nullptr;
+            void* ctx = nullptr;
+            {
+                std::unique_lock<std::mutex> lk(mu_);
+                cv_.wait(lk, [&] { return gen_ != seen; });
+                seen = gen_;
+                if (idx >= want_) continue;
+                body = body_;
+                ctx = ctx_;
+            }
+            body(ctx);
+            std::lock_guard<std::mutex> lk(mu_);
+            if (--pending_ == 0) done_cv_.notify_all();
+        }
+    }
+
+    std::mutex job_mu_;
+    std::mutex mu_;
+    std::condition_variable cv_, done_cv_;
+    uint64_t gen_ = 0;
+    int want_ = 0;
+    int pending_ = 0;
+    void (*body_)(void*) = nullptr;
+    void* ctx_ = nullptr;
+    std::vector<std::thread> threads_;
+};
+
 struct Job {
     int mode;
     const uint16_t* g16;
@@ -110,8 +210,9 @@ struct Job {
     std::atomic<int64_t> next{0};
 };
 
-void work(Job* job)
+void work(void* arg)
 {
+    Job* job = static_cast<Job*>(arg);
     float gbuf[kChunk]; // 64 KB on the thread's stack
     const int64_t nchunks = (job->n + kChunk - 1) / kChunk;
     for (int64_t c = job->next.fetch_add(1); c < nchunks; c = job->next.fetch_add(1)) {
@@ -154,18 +255,13 @@ extern "C" int zero_cpu_adam(const void* grad_fp16, float* master, float* m, flo
     job.s.bp1 = static_cast<float>(1.0 - std::pow(static_cast<double>(beta1), static_cast<double>(t - 1)));
     job.s.bp2 = static_cast<float>(1.0 - std::pow(static_cast<double>(beta2), static_cast<double>(t - 1)));
 
-    int nt = threads > 0 ? threads : static_cast<int>(std::thread::hardware_concurrency());
-    if (nt < 1) nt = 1;
+    HostPool& pool = HostPool::get();
+    int nt = threads > 0 ? threads : pool.size() + 1;
     const int64_t nchunks = (n + kChunk - 1) / kChunk;
     if (nt > nchunks) nt = static_cast<int>(nchunks);
-    std::vector<std::thread> pool;
-    try {
-        pool.reserve(static_cast<size_t>(nt - 1));
-        for (int k = 1; k < nt; ++k) pool.emplace_back(work, &job);
-    } catch (...) {
-        // fewer helpers than asked: the chunks still all get done
-    }
-    work(&job); // the calling thread works too
-    for (auto& th : pool) th.join();
+    if (nt <= 1)
+        work(&job);
+    else
+        pool.run(nt - 1, work, &job); // the calling thread works too
     return ZERO_OK;
 }
