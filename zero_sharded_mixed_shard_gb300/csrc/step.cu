@@ -995,9 +995,9 @@ extern "C" int zero_adam_step_bucketed(const void* grads_fp16, int64_t rank_stri
 }
 
 // ---------------------------------------------------------------------------
-// ZeRO-Offload: the GPU forms the gradient mean and sends it to the host as
-// fp16; a host function runs the CPU Adam of each shard in stream order and
-// the shard's fp16 weights are copied back into the gathered vector.
+// ZeRO-Offload's GPU side: the gradient mean of the ranks, rounded to fp16,
+// written to device or page-locked host memory (the host side and the
+// pipelined step are in offload.cu)
 // ---------------------------------------------------------------------------
 
 namespace {
@@ -1043,83 +1043,6 @@ KernelFn pick_reduce_kernel(int V, int P)
     }
 }
 
-// The CPU update of every shard, run by the CUDA driver in stream order.
-// The shards are contiguous, so one dynamically scheduled pass of the host
-// threads over [0, N) updates every rank's shard ([P3] §2.3 gives each
-// GPU's shard to CPU workers); chunks go to whichever thread is free.
-struct OffloadUpdate {
-    const void* g16;
-    float* w;
-    float* m;
-    float* v;
-    void* p16;
-    int64_t N;
-    int64_t t;
-    float lr, b1, b2, eps;
-    int32_t mode;
-    int32_t threads;
-};
-
-void CUDART_CB offload_update(void* arg)
-{
-    OffloadUpdate* u = static_cast<OffloadUpdate*>(arg);
-    // the arguments were validated when the step was enqueued
-    (void)zero_cpu_adam(u->g16, u->w, u->m, u->v, u->p16, u->N, u->t, u->lr, u->b1, u->b2, u->eps, u->mode,
-                        u->threads);
-    delete u;
-}
-
-// The offload step runs as a pipeline over pieces of the vector (groups of
-// whole shards): the GPU reduces piece j+1 while the host updates piece j
-// and piece j-1's weights cross back.  Host functions run on one internal
-// stream and the weight copies on another, one pair per device, created on
-// first use and kept; events order the three streams.
-constexpr int kOffloadPieces = 16;
-constexpr int64_t kOffloadMinPiece = int64_t(1) << 20; // elements
-
-struct OffloadStreams {
-    cudaStream_t host = nullptr;
-    cudaStream_t copy = nullptr;
-};
-
-int offload_streams(OffloadStreams* out)
-{
-    static std::mutex mu;
-    static OffloadStreams table[64];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return record_cuda(e);
-    if (dev < 0 || dev >= 64) return ZERO_EINVAL;
-    std::lock_guard<std::mutex> lk(mu);
-    OffloadStreams& s = table[dev];
-    if (!s.host) {
-        cudaStream_t h = nullptr, c = nullptr;
-        e = cudaStreamCreateWithFlags(&h, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c, cudaStreamNonBlocking);
-        if (e != cudaSuccess) {
-            if (h) cudaStreamDestroy(h);
-            return record_cuda(e);
-        }
-        s.host = h;
-        s.copy = c;
-    }
-    *out = s;
-    return ZERO_OK;
-}
-
-// `waiter` waits for the work enqueued so far on `src` (a fresh event each
-// time; destroying it at once is allowed, the wait stays enqueued).
-cudaError_t stream_after(cudaStream_t waiter, cudaStream_t src)
-{
-    cudaEvent_t ev;
-    cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-    if (e != cudaSuccess) return e;
-    e = cudaEventRecord(ev, src);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(waiter, ev, 0);
-    cudaEventDestroy(ev);
-    return e;
-}
-
 } // namespace
 
 extern "C" int zero_reduce_scatter_fp16(const void* grads_fp16, int64_t rank_stride, int64_t grad_offset,
@@ -1158,79 +1081,6 @@ extern "C" int zero_reduce_scatter_fp16(const void* grads_fp16, int64_t rank_str
     fn<<<static_cast<unsigned int>(blocks), kThreads, 0, static_cast<cudaStream_t>(cuda_stream)>>>(a);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ZERO_OK : record_cuda(e);
-}
-
-extern "C" int zero_offload_step(const void* grads_fp16, int64_t rank_stride, float* master_host, float* m_host,
-                                 float* v_host, void* grad16_host, void* params16_host, void* params_fp16,
-                                 int64_t N, int32_t P, int32_t stage, int64_t t, float lr, float beta1,
-                                 float beta2, float eps, int32_t mode, int32_t cpu_threads, void* cuda_stream)
-{
-    int rc = check_scalars(N, P, stage, t, lr, beta1, beta2, eps, mode);
-    if (rc) return rc;
-    if (rank_stride < N || cpu_threads < 0 || cpu_threads > 1024) return ZERO_EINVAL;
-    if (mode > ZERO_MODE_FOLDED_STORAGE) return ZERO_EINVAL; // the host update is Adam
-    if (!grads_fp16 || !master_host || !m_host || !v_host || !grad16_host || !params16_host || !params_fp16)
-        return ZERO_EINVAL;
-    if (reinterpret_cast<uintptr_t>(master_host) % 4 || reinterpret_cast<uintptr_t>(m_host) % 4 ||
-        reinterpret_cast<uintptr_t>(v_host) % 4 || reinterpret_cast<uintptr_t>(params16_host) % 2 ||
-        reinterpret_cast<uintptr_t>(params_fp16) % 2)
-        return ZERO_EALIGN;
-    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-    OffloadStreams side;
-    rc = offload_streams(&side);
-    if (rc) return rc;
-    const int64_t M = N / P + (N % P != 0);
-    const auto shard_begin = [&](int64_t k) { return k * M < N ? k * M : N; };
-    int64_t pieces = P < kOffloadPieces ? P : kOffloadPieces;
-    const int64_t by_size = (N + kOffloadMinPiece - 1) / kOffloadMinPiece;
-    if (pieces > by_size) pieces = by_size;
-    const uint16_t* g16 = static_cast<const uint16_t*>(grad16_host);
-    uint16_t* p16 = static_cast<uint16_t*>(params16_host);
-    __half* params = static_cast<__half*>(params_fp16);
-
-    cudaError_t ce = cudaSuccess;
-    for (int64_t j = 0; j < pieces && ce == cudaSuccess && rc == ZERO_OK; ++j) {
-        const int64_t k0 = j * P / pieces, k1 = (j + 1) * P / pieces;
-        const int64_t b = shard_begin(k0), e = shard_begin(k1);
-        if (b >= e) continue;
-        // 1. the GPU side of every rank: the fp16 gradient mean of the piece
-        //    lands in host memory
-        rc = zero_reduce_scatter_fp16(grads_fp16, rank_stride, b, P, e - b, const_cast<uint16_t*>(g16) + b,
-                                      cuda_stream);
-        if (rc) break;
-        // 2. the host update of the piece, once its gradients have arrived
-        ce = stream_after(side.host, stream);
-        if (ce != cudaSuccess) break;
-        OffloadUpdate* u = new (std::nothrow) OffloadUpdate{g16 + b, master_host + b, m_host + b, v_host + b,
-                                                            p16 + b, e - b, t, lr, beta1, beta2, eps, mode,
-                                                            cpu_threads};
-        if (!u) {
-            rc = ZERO_ENOMEM;
-            break;
-        }
-        ce = cudaLaunchHostFunc(side.host, offload_update, u);
-        if (ce != cudaSuccess) {
-            delete u;
-            break;
-        }
-        // 3. the all-gather: shard k's fp16 weights at offset kM of the device vector
-        ce = stream_after(side.copy, side.host);
-        for (int64_t k = k0; k < k1 && ce == cudaSuccess; ++k) {
-            const int64_t sb = shard_begin(k), se = shard_begin(k + 1);
-            if (sb < se)
-                ce = cudaMemcpyAsync(params + sb, p16 + sb, static_cast<size_t>(se - sb) * 2,
-                                     cudaMemcpyHostToDevice, side.copy);
-        }
-    }
-    // the caller's stream passes this step only when all of it is done (also
-    // after a failure part-way, for what was enqueued)
-    const cudaError_t j1 = stream_after(stream, side.host);
-    const cudaError_t j2 = stream_after(stream, side.copy);
-    if (rc) return rc;
-    if (ce != cudaSuccess) return record_cuda(ce);
-    if (j1 != cudaSuccess) return record_cuda(j1);
-    if (j2 != cudaSuccess) return record_cuda(j2);
-    return ZERO_OK;
 }
 
 extern "C" int zero_selftest_wait_timeout(const void* grads_fp16, int64_t rank_stride, float* master,
@@ -1292,6 +1142,13 @@ extern "C" int zero_device_timeouts(int64_t* count, int32_t reset)
 __attribute__((visibility("hidden"))) int zero_record_cuda_error(int err)
 {
     return record_cuda(static_cast<cudaError_t>(err));
+}
+
+__attribute__((visibility("hidden"))) int zero_check_step_scalars(int64_t N, int32_t P, int32_t stage, int64_t t,
+                                                                  float lr, float b1, float b2, float eps,
+                                                                  int32_t mode)
+{
+    return check_scalars(N, P, stage, t, lr, b1, b2, eps, mode);
 }
 
 extern "C" int zero_last_cuda_error(void) { return g_last_cuda_error; }
