@@ -451,3 +451,46 @@ def test_step_max_sms_leaves_results_unchanged(z, cap):
     finally:
         assert z.zero_set_step_max_sms(prev) == cap
     assert z.zero_device_timeouts() == 0
+
+
+def test_concurrent_callers_on_two_streams(z):
+    """Two host threads enqueue steps of two different problems on two
+    streams at once (one takes the bulk pipeline, one the vector path); the
+    library's per-kernel set-up is shared between them, and each result must
+    still equal the oracle bit for bit."""
+    import threading
+
+    problems = [(8, _tma_size(4101)), (5, 70_001)]
+    cases = []
+    for k, (P, N) in enumerate(problems):
+        stride = synth.round_up(N, 8)
+        w0, m0, v0, p0 = synth.np_state(N, 80 + k)
+        codes = [synth.np_grads(P, N, stride, 1e-3, 81 + 10 * k + t) for t in (1, 2, 3)]
+        cases.append(dict(P=P, N=N, stride=stride, init=(w0, m0, v0, p0), codes=codes,
+                          state=dev_state(w0, m0, v0, p0), grads=[dev_u16(c) for c in codes],
+                          stream=torch.cuda.Stream()))
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(c):
+        try:
+            for t in (1, 2, 3):
+                z.zero_adam_step(c["grads"][t - 1], c["stride"], *c["state"], c["N"], c["P"], 2, t,
+                                 LR, B1, B2, EPS, 0, c["stream"])
+        except Exception as e:   # pragma: no cover - reported below
+            errors.append(e)
+
+    ths = [threading.Thread(target=run, args=(c,)) for c in cases]
+    for th in ths:
+        th.start()
+    for th in ths:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors
+    for c in cases:
+        w0, m0, v0, _ = c["init"]
+        ref = [w0.copy(), m0.copy(), v0.copy()]
+        for t in (1, 2, 3):
+            p_ref = oracle.adam_elems(c["codes"][t - 1], c["stride"], c["P"], *ref, t, LR, B1, B2,
+                                      EPS, 0, threads=8)
+        assert max_ulps(host_state(c["state"]), ref + [p_ref]) == (0, 0), c["P"]
