@@ -279,6 +279,22 @@ int zero_adam_step_bucketed(const void* grads_fp16, int64_t rank_stride, float* 
  * thread-safe (atomic).  Errors: ZERO_EINVAL (max_sms < 0). */
 int zero_set_step_max_sms(int32_t max_sms, int32_t* previous);
 
+/* Which kernel zero_adam_step would launch for these arguments (a
+ * diagnostic with no counterpart on the pages; nothing is launched).
+ * *kernel = ZERO_KERNEL_BULK for the bulk-copy pipeline (one CTA per SM,
+ * used when every buffer shares one 16-byte phase and there are at least 4
+ * tiles of 2048 elements per SM) or ZERO_KERNEL_VECTOR for the vector
+ * kernel; *vector_width = the elements of one access (8 on the pipeline,
+ * else 8, 4, 2 or 1 by alignment); *ctas = the CTAs of the launch.  Depends
+ * on the current device's SM count and on zero_set_step_max_sms.
+ * Errors: as zero_adam_step (the hyper-parameters are not taken), and
+ * ZERO_EINVAL for a null output pointer. */
+#define ZERO_KERNEL_BULK 1
+#define ZERO_KERNEL_VECTOR 2
+int zero_step_plan(const void* grads_fp16, int64_t rank_stride, float* master, float* m, float* v,
+                   void* params_fp16, int64_t N, int32_t P, int32_t stage, int32_t mode,
+                   int32_t* kernel, int32_t* vector_width, int64_t* ctas);
+
 /* ------------------------------------------------------------------------ */
 /* ZeRO-Offload ([P3] §2.2 Offload 策略: the data-flow graph is cut along    */
 /* the fp16 gradient and fp16 parameter edges, so the parameter update and   */

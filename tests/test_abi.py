@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(zlib):
 def test_status_codes_match_header(zlib):
     text = "".join(open(h).read() for h in HEADERS)
     for name in ("ZERO_OK", "ZERO_EINVAL", "ZERO_EALIGN", "ZERO_EOVERLAP", "ZERO_ECUDA",
-                 "ZERO_ENOMEM", "ZERO_MAX_RANKS"):
+                 "ZERO_ENOMEM", "ZERO_MAX_RANKS", "ZERO_KERNEL_BULK", "ZERO_KERNEL_VECTOR"):
         m = re.search(r"#define\s+%s\s+\(?(-?\d+)\)?" % name, text)
         assert m and int(m.group(1)) == getattr(zlib, name), name
     for code in (0, -1, -2, -3, -4, -5):

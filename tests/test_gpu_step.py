@@ -115,6 +115,7 @@ def test_special_values(z):
         for t in (1, 2, 7):
             ref = [w0.copy(), m0.copy(), v0.copy()]
             s = dev_state(w0, m0, v0, np.zeros(N, np.uint16))
+            _assert_path(z, "vector", dev_u16(codes), N, s, N, P, mode)
             gpu_step(z, dev_u16(codes), N, s, N, P, t, mode)
             p_ref = oracle.adam_elems(codes, N, P, *ref, t, LR, B1, B2, EPS, mode)
             assert_close(host_state(s), ref + [p_ref], f"mode={mode} t={t}")
@@ -148,6 +149,7 @@ def test_special_state_values(z, big):
         for t in (1, 3):
             ref = [w0.copy(), m0.copy(), v0.copy()]
             s = dev_state(w0, m0, v0, np.zeros(N, np.uint16))
+            _assert_path(z, "bulk" if big else "vector", dev_u16(codes), N, s, N, P, mode)
             gpu_step(z, dev_u16(codes), N, s, N, P, t, mode)
             p_ref = oracle.adam_elems(codes, N, P, *ref, t, LR, B1, B2, EPS, mode, threads=8)
             assert_close(host_state(s), ref + [p_ref], f"mode={mode} t={t} big={big}")
@@ -324,15 +326,22 @@ def test_validation_with_device_buffers(z):
 # ---------------------------------------------------------------------------
 
 def _tma_size(extra):
+    """Enough 2048-element tiles for the bulk-copy pipeline: it is chosen
+    from 4 tiles per SM on."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    return sms * 2048 * 2 + extra
+    return sms * 2048 * 4 + extra
+
+
+def _assert_path(z, kernel, g, stride, s, N, P, mode=0):
+    plan = z.zero_step_plan(g, stride, *s, N, P, 2, mode)
+    assert plan["kernel"] == kernel, plan
 
 
 @pytest.mark.parametrize("P", [1, 3, 4, 8, 13, 16, 33, 64])
 def test_tma_path_matches_oracle(z, P):
     """P that fills whole 8-rank chunks and P that leaves a partial last chunk;
     a ragged tail of 5 elements; three steps of every mode."""
-    N = _tma_size(4101)            # 512 full tiles on 152 SMs, a partial tile, a tail of 5
+    N = _tma_size(4101)            # 4 x SMs full tiles, 2 more, a partial tile, a tail of 5
     stride = synth.round_up(N, 8) + 8
     worst = (0, 0)
     for mode in (0, 1, 2):
@@ -346,6 +355,7 @@ def test_tma_path_matches_oracle(z, P):
             p_ref = oracle.adam_elems(codes, stride, P, *ref, t, LR, B1, B2, EPS, mode, threads=8)
             u = max_ulps(host_state(s), ref + [p_ref])
             worst = (max(worst[0], u[0]), max(worst[1], u[1]))
+        _assert_path(z, "bulk", dev_u16(codes), stride, s, N, P, mode)
     assert worst == (0, 0), f"P={P}: max ulp {worst}"
     assert z.zero_device_timeouts() == 0
 
@@ -368,6 +378,7 @@ def test_tma_path_with_head(z, head):
         bufs.append(b[head: head + N])
     p_buf = torch.zeros(N + 8, dtype=torch.int16, device="cuda")
     params = p_buf.view(torch.float16)[head: head + N]
+    _assert_path(z, "bulk", g, stride, bufs + [params], N, P)
     z.zero_adam_step(g, stride, *bufs, params, N, P, 2, 1, LR, B1, B2, EPS, 0)
     ref = [w0.copy(), m0.copy(), v0.copy()]
     p_ref = oracle.adam_elems(codes, stride, P, *ref, 1, LR, B1, B2, EPS, 0, threads=8)
@@ -384,10 +395,12 @@ def test_tma_and_vector_paths_agree(z):
     g = dev_u16(codes)
     w0, m0, v0, p0 = synth.np_state(N, 4)
     a = dev_state(w0, m0, v0, p0)
+    _assert_path(z, "bulk", g, stride, a, N, P)
     gpu_step(z, g, stride, a, N, P, 2, 0)
     b = dev_state(w0, m0, v0, p0)
     p_buf = torch.zeros(N + 1, dtype=torch.int16, device="cuda")
     b[3] = p_buf.view(torch.float16)[1:]
+    _assert_path(z, "vector", g, stride, b, N, P)
     gpu_step(z, g, stride, b, N, P, 2, 0)
     for x, y in zip(host_state(a), host_state(b)):
         assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
@@ -410,6 +423,8 @@ def test_sgd_and_momentum_match_oracle(z, mode, big):
     m0 = (np.random.default_rng(1).standard_normal(N) * 1e-3).astype(np.float32)
     ref = [w0.copy(), m0.copy(), v0.copy()]
     s = dev_state(w0, m0, v0, p0)
+    _assert_path(z, "bulk" if big else "vector", dev_u16(synth.np_grads(P, N, stride, 1e-3, 1)),
+                 stride, s, N, P, mode)
     sentinel = torch.full((N,), 1234.5, device="cuda")
     for t in range(1, 5):
         codes = synth.np_grads(P, N, stride, 1e-3, 500 + t, heavy_tail_frac=0.01)
@@ -494,3 +509,36 @@ def test_concurrent_callers_on_two_streams(z):
             p_ref = oracle.adam_elems(c["codes"][t - 1], c["stride"], c["P"], *ref, t, LR, B1, B2,
                                       EPS, 0, threads=8)
         assert max_ulps(host_state(c["state"]), ref + [p_ref]) == (0, 0), c["P"]
+
+
+def test_step_plan_names_the_kernel(z):
+    """The diagnostic agrees with the dispatch rule: the bulk pipeline for
+    aligned problems of at least 4 tiles per SM (one CTA per SM, or the SM
+    cap), the vector kernel below that or off the 16-byte phase."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    P = 8
+
+    def bufs(N, p_off=0):
+        g = torch.zeros((P, synth.round_up(N, 8)), dtype=torch.float16, device="cuda")
+        st = [torch.zeros(N, device="cuda") for _ in range(3)]
+        p = torch.zeros(N + 8, dtype=torch.float16, device="cuda")[p_off:p_off + N]
+        return g, st, p
+
+    big = sms * 2048 * 4
+    g, st, p = bufs(big)
+    plan = z.zero_step_plan(g, g.shape[1], *st, p, big, P, 1, 0)
+    assert plan == {"kernel": "bulk", "vector_width": 8, "ctas": sms}
+    small = big - 2048
+    g, st, p = bufs(small)
+    plan = z.zero_step_plan(g, g.shape[1], *st, p, small, P, 1, 0)
+    assert plan["kernel"] == "vector" and plan["vector_width"] == 8
+    g, st, p = bufs(big, p_off=1)          # parameters one half off the others' phase
+    plan = z.zero_step_plan(g, g.shape[1], *st, p, big, P, 1, 0)
+    assert plan["kernel"] == "vector" and plan["vector_width"] == 1
+    prev = z.zero_set_step_max_sms(10)
+    try:
+        g, st, p = bufs(big)
+        plan = z.zero_step_plan(g, g.shape[1], *st, p, big, P, 1, 0)
+        assert plan == {"kernel": "bulk", "vector_width": 8, "ctas": 10}
+    finally:
+        z.zero_set_step_max_sms(prev)

@@ -65,6 +65,9 @@ def run_workload(z, wl, mode, steps, check_steps):
     stride = wl.rank_stride(True)
     g = torch.empty((P, stride), dtype=torch.float16, device=dev)
     master, m, v, params = synth.torch_state(E, wl.seed, dev, wl.master_sigma)
+    # the full-size workloads run the bulk-copy pipeline, as in the benchmark
+    plan = z.zero_step_plan(g, stride, master, m, v, params, E, P, wl.stage, mode)
+    assert plan["kernel"] == "bulk", (wl.name, plan)
     wins = windows(wl, wl.seed)
     ref = {w: [master[w[0]:w[1]].cpu().numpy(), m[w[0]:w[1]].cpu().numpy(),
                v[w[0]:w[1]].cpu().numpy()] for w in wins}

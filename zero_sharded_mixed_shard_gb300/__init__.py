@@ -23,6 +23,8 @@ ZERO_EOVERLAP = -3
 ZERO_ECUDA = -4
 ZERO_ENOMEM = -5
 ZERO_MAX_RANKS = 1024
+ZERO_KERNEL_BULK = 1
+ZERO_KERNEL_VECTOR = 2
 
 MODE_STANDARD = 0
 MODE_FOLDED_LITERAL = 1
@@ -33,7 +35,8 @@ MODE_MOMENTUM = 4
 # every symbol include/zero_step.h declares
 EXPORTED = ("zero_init_layout", "zero_free_layout", "zero_shard_range", "zero_memory_bytes",
             "zero_adam_step", "zero_adam_step_shard", "zero_plan_buckets", "zero_adam_step_range",
-            "zero_adam_step_bucketed", "zero_set_step_max_sms", "zero_reduce_scatter_fp16", "zero_cpu_adam",
+            "zero_adam_step_bucketed", "zero_set_step_max_sms", "zero_step_plan",
+            "zero_reduce_scatter_fp16", "zero_cpu_adam",
             "zero_offload_step", "zero_mlp4_loss", "zero_mlp4_layer_grads",
             "zero_mlp4_zero3_step", "zero_mlp4_zero3_step_noalloc", "zero_device_timeouts",
             "zero_selftest_wait_timeout", "zero_strerror",
@@ -114,6 +117,10 @@ def lib() -> ctypes.CDLL:
                                           f32, f32, f32, f32, i32, ctypes.POINTER(zero_bucket_t),
                                           i32, ctypes.POINTER(ctypes.c_void_p), vp]
     L.zero_adam_step_bucketed.restype = ctypes.c_int
+    L.zero_step_plan.argtypes = [vp, i64, vp, vp, vp, vp, i64, i32, i32, i32,
+                                 ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                 ctypes.POINTER(ctypes.c_int64)]
+    L.zero_step_plan.restype = ctypes.c_int
     L.zero_set_step_max_sms.argtypes = [i32, ctypes.POINTER(ctypes.c_int32)]
     L.zero_set_step_max_sms.restype = ctypes.c_int
     L.zero_reduce_scatter_fp16.argtypes = [vp, i64, i64, i32, i64, vp, vp]
@@ -250,6 +257,20 @@ def zero_set_step_max_sms(max_sms: int) -> int:
     if rc:
         raise ZeroError(rc, "zero_set_step_max_sms")
     return prev.value
+
+
+def zero_step_plan(grads, rank_stride: int, master, m, v, params, N: int, P: int, stage: int,
+                   mode: int) -> dict:
+    """The kernel zero_adam_step would launch: {"kernel": "bulk" | "vector",
+    "vector_width": V, "ctas": C} (nothing is launched)."""
+    k, vw, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
+    rc = lib().zero_step_plan(_addr(grads), rank_stride, _addr(master), _addr(m), _addr(v),
+                              _addr(params), N, P, stage, mode, ctypes.byref(k), ctypes.byref(vw),
+                              ctypes.byref(c))
+    if rc:
+        raise ZeroError(rc, "zero_step_plan")
+    return {"kernel": "bulk" if k.value == ZERO_KERNEL_BULK else "vector",
+            "vector_width": vw.value, "ctas": c.value}
 
 
 def zero_device_timeouts(reset: bool = False) -> int:

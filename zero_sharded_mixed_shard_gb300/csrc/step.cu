@@ -813,30 +813,16 @@ long long bulk_tiles(const StepArgs& a)
     return ((a.n - a.head) / 8 * 8 + kTile - 1) / kTile;
 }
 
-int launch_tma(const StepArgs& a, int mode, int sms, cudaStream_t stream)
-{
-    const TmaKernel k = pick_tma_kernel(mode, a.P);
-    const int rc = kernel_setup(k.fn, true);
-    if (rc < 0) return rc;
-    k.fn<<<static_cast<unsigned int>(sms), k.threads, kBulkSmem, stream>>>(a);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? ZERO_OK : record_cuda(e);
-}
-
-int launch_vector(const StepArgs& a, int V, int mode, int sms, cudaStream_t stream)
-{
-    KernelFn fn = pick_kernel(mode, V, a.P);
-    const int per_sm = kernel_setup(fn, false);
-    if (per_sm < 0) return per_sm;
-    const long long body = (a.n - a.head) / V;
-    long long blocks = (body + kThreads - 1) / kThreads;
-    const long long cap = static_cast<long long>(sms) * per_sm;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    fn<<<static_cast<unsigned int>(blocks), kThreads, 0, stream>>>(a);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? ZERO_OK : record_cuda(e);
-}
+// What a step of the range will launch: the kernel, its vector width and
+// its grid.  Decided once, by plan_range, for both the launch and the
+// zero_step_plan diagnostic.
+struct LaunchPlan {
+    bool bulk = false; // the bulk-copy pipeline, else the vector kernel
+    int V = 1;         // elements per vector access (8 on the pipeline)
+    long long ctas = 0;
+    int threads = 0;
+    KernelFn fn = nullptr;
+};
 
 // The bulk-copy pipeline needs every stream on one 16-byte phase (V = 8) and
 // pays off once every SM has a few tiles; smaller or misaligned problems take
@@ -847,8 +833,7 @@ constexpr int kMinTilesPerSm = 4;
 // enqueued.  Below the SM count it leaves SMs free for work on other streams.
 std::atomic<int> g_step_max_sms{0};
 
-int launch_range(StepArgs a, int64_t t, float lr, float b1, float b2, float eps, int mode,
-                 cudaStream_t stream)
+int plan_range(StepArgs& a, int64_t t, float lr, float b1, float b2, float eps, int mode, LaunchPlan* plan)
 {
     int V = 1;
     int rc = prepare_range(a, t, lr, b1, b2, eps, mode, &V);
@@ -857,9 +842,58 @@ int launch_range(StepArgs a, int64_t t, float lr, float b1, float b2, float eps,
     if (sms <= 0) return record_cuda(cudaGetLastError());
     const int cap = g_step_max_sms.load(std::memory_order_relaxed);
     if (cap > 0 && cap < sms) sms = cap;
-    if (V == 8 && bulk_tiles(a) >= static_cast<long long>(kMinTilesPerSm) * sms)
-        return launch_tma(a, mode, sms, stream);
-    return launch_vector(a, V, mode, sms, stream);
+    plan->V = V;
+    if (V == 8 && bulk_tiles(a) >= static_cast<long long>(kMinTilesPerSm) * sms) {
+        const TmaKernel k = pick_tma_kernel(mode, a.P);
+        rc = kernel_setup(k.fn, true);
+        if (rc < 0) return rc;
+        plan->bulk = true;
+        plan->fn = k.fn;
+        plan->threads = k.threads;
+        plan->ctas = sms;
+        return ZERO_OK;
+    }
+    KernelFn fn = pick_kernel(mode, V, a.P);
+    const int per_sm = kernel_setup(fn, false);
+    if (per_sm < 0) return per_sm;
+    const long long body = (a.n - a.head) / V;
+    long long blocks = (body + kThreads - 1) / kThreads;
+    const long long limit = static_cast<long long>(sms) * per_sm;
+    if (blocks > limit) blocks = limit;
+    if (blocks < 1) blocks = 1;
+    plan->bulk = false;
+    plan->fn = fn;
+    plan->threads = kThreads;
+    plan->ctas = blocks;
+    return ZERO_OK;
+}
+
+int launch_plan(const StepArgs& a, const LaunchPlan& plan, cudaStream_t stream)
+{
+    plan.fn<<<static_cast<unsigned int>(plan.ctas), plan.threads, plan.bulk ? kBulkSmem : 0, stream>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : record_cuda(e);
+}
+
+// The bulk-copy pipeline on one CTA per SM, whatever the problem size (the
+// bounded-wait diagnostic).
+int launch_tma(const StepArgs& a, int mode, int sms, cudaStream_t stream)
+{
+    const TmaKernel k = pick_tma_kernel(mode, a.P);
+    const int rc = kernel_setup(k.fn, true);
+    if (rc < 0) return rc;
+    k.fn<<<static_cast<unsigned int>(sms), k.threads, kBulkSmem, stream>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : record_cuda(e);
+}
+
+int launch_range(StepArgs a, int64_t t, float lr, float b1, float b2, float eps, int mode,
+                 cudaStream_t stream)
+{
+    LaunchPlan plan;
+    const int rc = plan_range(a, t, lr, b1, b2, eps, mode, &plan);
+    if (rc) return rc;
+    return launch_plan(a, plan, stream);
 }
 
 } // namespace
@@ -869,6 +903,34 @@ extern "C" int zero_set_step_max_sms(int32_t max_sms, int32_t* previous)
     if (max_sms < 0) return ZERO_EINVAL;
     const int old = g_step_max_sms.exchange(max_sms, std::memory_order_relaxed);
     if (previous) *previous = old;
+    return ZERO_OK;
+}
+
+extern "C" int zero_step_plan(const void* grads_fp16, int64_t rank_stride, float* master, float* m, float* v,
+                              void* params_fp16, int64_t N, int32_t P, int32_t stage, int32_t mode,
+                              int32_t* kernel, int32_t* vector_width, int64_t* ctas)
+{
+    if (!kernel || !vector_width || !ctas) return ZERO_EINVAL;
+    // the hyper-parameters do not enter the choice: any valid ones will do
+    const float lr = 1e-3f, b1 = 0.9f, b2 = 0.999f, eps = 1e-8f;
+    int rc = check_scalars(N, P, stage, 1, lr, b1, b2, eps, mode);
+    if (rc) return rc;
+    if (rank_stride < N) return ZERO_EINVAL;
+    StepArgs a{};
+    a.g = static_cast<const __half*>(grads_fp16);
+    a.stride = rank_stride;
+    a.w = master;
+    a.m = m;
+    a.v = v;
+    a.p = static_cast<__half*>(params_fp16);
+    a.n = N;
+    a.P = P;
+    LaunchPlan plan;
+    rc = plan_range(a, 1, lr, b1, b2, eps, mode, &plan);
+    if (rc) return rc;
+    *kernel = plan.bulk ? ZERO_KERNEL_BULK : ZERO_KERNEL_VECTOR;
+    *vector_width = plan.V;
+    *ctas = plan.ctas;
     return ZERO_OK;
 }
 
