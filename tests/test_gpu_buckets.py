@@ -77,8 +77,11 @@ def test_bucketed_step_waits_for_each_bucket(z, P, mode):
 
 
 def test_range_steps_equal_whole_step(z):
+    """Cuts at odd offsets: the ranges take the vector kernel and, for the
+    longest one (about 6 tiles per SM, starting off a 16-byte boundary), the
+    bulk pipeline with a head of elements done one by one."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    P, N = 8, sms * 2048 * 6 + 77
+    P, N = 8, sms * 2048 * 12 + 77
     stride = synth.round_up(N, 8)
     g = synth.torch_grads(P, N, stride, 1e-3, 3, "cuda")
     base = synth.torch_state(N, 3, "cuda")
@@ -86,7 +89,11 @@ def test_range_steps_equal_whole_step(z):
     z.zero_adam_step(g, stride, *whole, N, P, 2, 2, LR, B1, B2, EPS, 0)
     parts = [x.clone() for x in base]
     cuts = sorted({0, N, 1, 12_345, 12_346, N // 3, N // 3 + 5, N // 2 + 1, N - 9})
+    kernels = set()
     for b, e in zip(cuts, cuts[1:]):
+        plan = z.zero_step_plan(g[:, b:], stride, *[x[b:] for x in parts], e - b, P, 2, 0)
+        kernels.add(plan["kernel"])
         z.zero_adam_step_range(g, stride, b, e, *parts, N, P, 2, 2, LR, B1, B2, EPS, 0)
+    assert kernels == {"bulk", "vector"}
     for x, y in zip(whole, parts):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
