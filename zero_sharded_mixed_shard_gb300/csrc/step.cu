@@ -309,8 +309,17 @@ __device__ __forceinline__ void step_elems(const StepArgs& a, long long i)
     store_halves<V>(a.p + i, w); // all-gather: element i of the full vector
 }
 
+// Resident CTAs per SM the vector kernel is compiled for (its registers
+// then fit 4 CTAs of 256 threads).  Measured on GB300 with L2 flushed: for
+// P = 4, 8 and the generic instance, problems that need more than one wave
+// at the default 3 CTAs per SM gain 8-22 % (1 M elements: P = 4 13.9 ->
+// 12.8 us, P = 13 23.0 -> 18.0 us) and smaller ones are unchanged; for
+// P = 16 the register cap costs up to 18 %, so the wider instances keep
+// their registers.
+constexpr int vector_min_blocks(int PT) { return PT == 0 || PT <= 8 ? 4 : 1; }
+
 template <int MODE, int V, int PT>
-__global__ void __launch_bounds__(kThreads) zero_fused_step_kernel(const StepArgs a)
+__global__ void __launch_bounds__(kThreads, vector_min_blocks(PT)) zero_fused_step_kernel(const StepArgs a)
 {
     const long long tid = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
     const long long nthreads = static_cast<long long>(gridDim.x) * kThreads;
