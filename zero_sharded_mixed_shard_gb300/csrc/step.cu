@@ -481,11 +481,30 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
     float* v0 = uses_v(MODE) ? a.v + a.head : nullptr;
     __half* p0 = a.p + a.head;
 
+    // (chunk, tile) of unit u.  With P known at compile time the division
+    // by the chunk count is a shift or a multiply; with P read at run time
+    // it would be a 64-bit division per unit, so the generic instance keeps
+    // counters instead (units are walked in order: the next chunk of the
+    // same tile, else chunk 0 of this CTA's next tile).  Measured: counters
+    // in the compile-time instances cost P = 16 and 64 20-25 %.
     auto tile_of = [&](long long u) { return blockIdx.x + (u / nch) * gridDim.x; };
-    auto issue = [&](long long u) { // thread 0 only
+    int issue_c = 0;                   // generic instance, thread 0: chunk of the next unit to issue
+    long long issue_tile = blockIdx.x; // and its tile
+    auto issue = [&](long long u) {    // thread 0 only, for u = 0, 1, 2, ... in turn
         const int s = static_cast<int>(u % kStages);
-        const int c = static_cast<int>(u % nch);
-        const long long i0 = tile_of(u) * kTile;
+        int c;
+        long long i0;
+        if constexpr (PT > 0) {
+            c = static_cast<int>(u % nch);
+            i0 = tile_of(u) * kTile;
+        } else {
+            c = issue_c;
+            i0 = issue_tile * kTile;
+            if (++issue_c == nch) {
+                issue_c = 0;
+                issue_tile += gridDim.x;
+            }
+        }
         const long long len = nbulk - i0 < kTile ? nbulk - i0 : kTile;
         const int rc = P - c * kChunkRanks < kChunkRanks ? P - c * kChunkRanks : kChunkRanks;
         const uint32_t hb = static_cast<uint32_t>(len) * 2, fb = static_cast<uint32_t>(len) * 4;
@@ -507,6 +526,8 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
 
     float acc[E], w[E], m[E] = {}, v[E] = {};
     long long u = 0;
+    int c_run = 0;                   // generic instance: chunk of ranks of unit u
+    long long tile_run = blockIdx.x; // and its tile
     bool failed = false;
     for (; u < units; ++u) {
         const int s = static_cast<int>(u % kStages);
@@ -518,8 +539,8 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
         }
         if (tid == 0 && u >= 1 && u - 1 + kStages < units) issue(u - 1 + kStages);
 
-        const int c = static_cast<int>(u % nch);
-        const long long i0 = tile_of(u) * kTile;
+        const int c = PT > 0 ? static_cast<int>(u % nch) : c_run;
+        const long long i0 = (PT > 0 ? tile_of(u) : tile_run) * kTile;
         const long long len = nbulk - i0 < kTile ? nbulk - i0 : kTile;
         const unsigned char* st = smem + static_cast<size_t>(s) * kStageBytes;
         const int e0 = tid * E;
@@ -533,9 +554,18 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
             }
             // ranks c*8 .. c*8+rc-1 of this tile, in rank order
             const int rc = P - c * kChunkRanks < kChunkRanks ? P - c * kChunkRanks : kChunkRanks;
+            if constexpr (PT > 0) {
 #pragma unroll
-            for (int q = 0; q < kChunkRanks; ++q)
-                if (q < rc) accumulate<E>(acc, smem_halves<E>(st + static_cast<size_t>(q) * kTile * 2 + e0 * 2));
+                for (int q = 0; q < kChunkRanks; ++q)
+                    if (q < rc) accumulate<E>(acc, smem_halves<E>(st + static_cast<size_t>(q) * kTile * 2 + e0 * 2));
+            } else {
+                // rc known only at run time: visit just the ranks present
+                // (measured against the predicated 8-slot form: P = 1 and 2
+                // gain 3-7 %, larger P about 1 %)
+#pragma unroll 1
+                for (int q = 0; q < rc; ++q)
+                    accumulate<E>(acc, smem_halves<E>(st + static_cast<size_t>(q) * kTile * 2 + e0 * 2));
+            }
             if (c == nch - 1) {
                 float gm[E];
                 bool special = false;
@@ -560,6 +590,12 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
                 if constexpr (uses_m(MODE)) store_floats<E>(m0 + i, m);
                 if constexpr (uses_v(MODE)) store_floats<E>(v0 + i, v);
                 store_halves<E>(p0 + i, w); // all-gather: element head + i of the full vector
+            }
+        }
+        if constexpr (PT == 0) {
+            if (++c_run == nch) {
+                c_run = 0;
+                tile_run += gridDim.x;
             }
         }
     }
@@ -650,16 +686,30 @@ TmaKernel tma_instance()
     return TmaKernel{zero_fused_step_tma_kernel<MODE, PT, NT, 2>, NT};
 }
 
+// Rank counts without an instance of their own, with P read at run time:
+// 1024 consumers up to 4 ranks, 512 above.
+template <int MODE, int NT>
+TmaKernel tma_generic()
+{
+    return TmaKernel{zero_fused_step_tma_kernel<MODE, 0, NT, 2>, NT};
+}
+
 template <int MODE>
 TmaKernel pick_tma_p(int P)
 {
     switch (P) {
+    case 1: return tma_instance<MODE, 1>();
+    case 2: return tma_instance<MODE, 2>();
     case 4: return tma_instance<MODE, 4>();
     case 8: return tma_instance<MODE, 8>();
     case 16: return tma_instance<MODE, 16>();
     case 32: return tma_instance<MODE, 32>();
     case 64: return tma_instance<MODE, 64>();
-    default: return tma_instance<MODE, 0>();
+    case 128: return tma_instance<MODE, 128>();
+    case 256: return tma_instance<MODE, 256>();
+    default: // measured: 256 consumers, as P = 8 takes, cost P = 5-7 20 %
+        if (P <= 4) return tma_generic<MODE, tma_threads(4)>();
+        return tma_generic<MODE, tma_threads(64)>();
     }
 }
 
