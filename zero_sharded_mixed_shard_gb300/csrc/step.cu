@@ -440,6 +440,16 @@ __device__ __forceinline__ void smem_floats(const unsigned char* p, float (&x)[E
     }
 }
 
+// acc += ranks 0..R-1 of a stage's gradient rows, in rank order (row q of
+// the stage holds rank c*8+q; `row` points at this thread's elements of
+// row 0, rows are kTile halves apart).
+template <int E, int R>
+__device__ __forceinline__ void accumulate_rows(float (&acc)[E], const unsigned char* row)
+{
+#pragma unroll
+    for (int q = 0; q < R; ++q) accumulate<E>(acc, smem_halves<E>(row + static_cast<size_t>(q) * kTile * 2));
+}
+
 // NT consumer threads, E = kTile / NT consecutive elements each per tile.
 template <int MODE, int PT, int NT, int G>
 __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepArgs a)
@@ -559,12 +569,19 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
                 for (int q = 0; q < kChunkRanks; ++q)
                     if (q < rc) accumulate<E>(acc, smem_halves<E>(st + static_cast<size_t>(q) * kTile * 2 + e0 * 2));
             } else {
-                // rc known only at run time: visit just the ranks present
-                // (measured against the predicated 8-slot form: P = 1 and 2
-                // gain 3-7 %, larger P about 1 %)
-#pragma unroll 1
-                for (int q = 0; q < rc; ++q)
-                    accumulate<E>(acc, smem_halves<E>(st + static_cast<size_t>(q) * kTile * 2 + e0 * 2));
+                // rc known only at run time (uniform over the CTA): one fully
+                // unrolled body per possible count
+                const unsigned char* row = st + static_cast<size_t>(e0) * 2;
+                switch (rc) {
+                case 8: accumulate_rows<E, 8>(acc, row); break;
+                case 7: accumulate_rows<E, 7>(acc, row); break;
+                case 6: accumulate_rows<E, 6>(acc, row); break;
+                case 5: accumulate_rows<E, 5>(acc, row); break;
+                case 4: accumulate_rows<E, 4>(acc, row); break;
+                case 3: accumulate_rows<E, 3>(acc, row); break;
+                case 2: accumulate_rows<E, 2>(acc, row); break;
+                default: accumulate_rows<E, 1>(acc, row); break;
+                }
             }
             if (c == nch - 1) {
                 float gm[E];
