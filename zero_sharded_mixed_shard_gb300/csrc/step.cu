@@ -15,12 +15,18 @@
 //    master copy and writes it back as fp16.
 //  高效AI 第19讲：分布式训练（第一部分） 通信原语: g = (1/N) Σ g_i.
 //
+// Also plain SGD and SGD with momentum (same pages, §（一） and §1.1.1), which
+// skip the state streams they do not use.
+//
 // The path is elementwise and HBM-bound (2P + 26 bytes moved per element
-// against about 15 fp32 operations), so there are no tensor cores here.  Each
-// thread owns V consecutive elements per iteration of a grid-stride loop:
-// one 16-byte load per rank for V = 8, two 16-byte loads per fp32 stream,
-// 16-byte stores.  Every arithmetic operation is an explicitly rounded fp32
-// intrinsic, so no multiply-add contraction can change a result.
+// against about 15 fp32 operations), so there are no tensor cores here.  Two
+// kernels: the bulk-copy pipeline (one CTA per SM, TMA bulk copies of whole
+// 4 KB rows into four shared-memory stages, bounded mbarrier waits) when
+// every stream shares one 16-byte phase and the problem has a few tiles per
+// SM, and a vector kernel (V consecutive elements per thread per iteration of
+// a grid-stride loop) for small or misaligned problems.  Every arithmetic
+// operation is an explicitly rounded fp32 intrinsic, so no multiply-add
+// contraction can change a result.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -29,8 +35,6 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
-#include <new>
-#include <thread>
 #include <type_traits>
 #include <utility>
 #include <vector>
