@@ -36,6 +36,12 @@
  *    are enqueued on the caller's stream and the call returns immediately.
  *  - Element counts and strides are in elements, not bytes.
  *  - fp16 buffers are passed as void* holding IEEE binary16 codes.
+ *  - zero_adam_step, zero_adam_step_shard and zero_adam_step_range enqueue
+ *    one kernel launch on the stream and nothing else.  The first call for a
+ *    kernel on a device also sets that kernel up (function attributes,
+ *    occupancy); after it, calls on a capturing stream are recorded into a
+ *    CUDA graph like any launch, and replaying the graph repeats the steps
+ *    with the arguments they were captured with (t included).
  */
 #ifndef ZERO_STEP_H
 #define ZERO_STEP_H
