@@ -9,15 +9,19 @@ F32_ULP_TOL = 2
 F16_ULP_TOL = 1
 
 
+# Floats mapped to integers in value order, one step per representable value,
+# with -0 one step below +0: a distance of 0 then means identical bits (NaN
+# payloads aside), so a zero of the wrong sign is caught.
 def _ordered32(x: np.ndarray) -> np.ndarray:
-    i = np.ascontiguousarray(x, np.float32).view(np.int32).astype(np.int64)
-    return np.where(i >= 0, i, -(1 << 31) - i)
+    i = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.int64)
+    mag = i & 0x7FFFFFFF
+    return np.where(i & 0x80000000, -mag - 1, mag)
 
 
 def _ordered16(codes: np.ndarray) -> np.ndarray:
     i = np.ascontiguousarray(codes).view(np.uint16).astype(np.int64)
     mag = i & 0x7FFF
-    return np.where(i & 0x8000, -mag, mag)
+    return np.where(i & 0x8000, -mag - 1, mag)
 
 
 def ulp32(a: np.ndarray, b: np.ndarray) -> int:

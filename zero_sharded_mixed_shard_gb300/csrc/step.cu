@@ -74,38 +74,46 @@ __device__ __forceinline__ float finish_mean(float sum, const StepArgs& a)
     if constexpr (PT > 0 && (PT & (PT - 1)) == 0) {
         return __fmul_rn(sum, 1.0f / static_cast<float>(PT));
     } else {
-        return a.p_pow2 ? __fmul_rn(sum, a.inv_p) : __fdiv_rn(sum, static_cast<float>(a.P));
+        if (a.p_pow2) return __fmul_rn(sum, a.inv_p);
+        return sum == 0.0f ? sum : __fdiv_rn(sum, static_cast<float>(a.P)); // +-0 / P = +-0
     }
 }
 
-// IEEE quotients whose operands are infinite are formed directly: CUDA's
-// correctly rounded divide and square root send such operands down a slow
-// path, and once the literal folded reading overflows v every element would
-// take it.  The results are the IEEE 754 ones.
-//   x / d for d positive and finite (the bias corrections): inf stays inf.
+// IEEE quotients whose operands are infinite or zero are formed directly:
+// CUDA's correctly rounded divide and square root are slow on such operands
+// (measured: the step on all-zero gradients and moments ran 2.6x slower),
+// and they are common -- once the literal folded reading overflows v every
+// element is infinite, and a parameter whose gradient and moments are still
+// exactly zero (an embedding row no batch has touched) has zero numerators.
+// The results are the IEEE 754 ones.
+//   x / d for d positive and finite (the bias corrections): inf stays inf,
+//   a zero stays the same zero.
 template <int G>
 __device__ __forceinline__ float div_by_positive(float x, float d)
 {
     if constexpr (G == 0) return __fdiv_rn(x, d);
-    return isinf(x) ? x : __fdiv_rn(x, d);
+    return (isinf(x) || x == 0.0f) ? x : __fdiv_rn(x, d); // inf / d = inf, +-0 / d = +-0
 }
 
 __device__ __forceinline__ bool is_pos_inf(float x) { return x == __int_as_float(0x7f800000); }
 
-//   sqrt(+inf) = +inf (every other input goes to the rounded square root).
+//   sqrt(+inf) = +inf, sqrt(+-0) = +-0 (every other input goes to the
+//   rounded square root).
 template <int G>
 __device__ __forceinline__ float sqrt_rn(float x)
 {
     if constexpr (G == 0) return __fsqrt_rn(x);
-    return is_pos_inf(x) ? x : __fsqrt_rn(x);
+    return (is_pos_inf(x) || x == 0.0f) ? x : __fsqrt_rn(x); // sqrt(+-0) = +-0
 }
 
-//   x / +inf: a zero carrying x's sign for finite x, NaN for infinite or NaN x.
+//   x / +inf: a zero carrying x's sign for finite x, NaN for infinite or NaN x;
+//   +-0 / d = +-0 for finite d > 0.
 template <int G>
 __device__ __forceinline__ float div_rn(float x, float d)
 {
     if constexpr (G == 0) return __fdiv_rn(x, d);
     if (is_pos_inf(d)) return isfinite(x) ? copysignf(0.0f, x) : __int_as_float(0x7fffffff);
+    if (x == 0.0f && d > 0.0f) return x; // +-0 / d = +-0 for d > 0 (finite here)
     return __fdiv_rn(x, d);
 }
 
@@ -303,9 +311,21 @@ __device__ __forceinline__ void step_elems(const StepArgs& a, long long i)
     }
 
 #pragma unroll
-    for (int j = 0; j < V; ++j) {
-        const float g = finish_mean<PT>(acc[j], a);
-        adam_elem<MODE>(a, g, w[j], m[j], v[j]);
+    for (int j = 0; j < V; ++j) acc[j] = finish_mean<PT>(acc[j], a); // the gradient means
+    // the shortcuts for infinite and zero operands only in warps that need
+    // them (the same warp-uniform dispatch as the bulk pipeline)
+    bool special = false;
+    if constexpr (MODE <= ZERO_MODE_FOLDED_STORAGE) {
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            special |= !(isfinite(acc[j]) && isfinite(m[j]) && isfinite(v[j])) || acc[j] == 0.0f;
+    }
+    if (__any_sync(__activemask(), special)) {
+#pragma unroll
+        for (int j = 0; j < V; ++j) adam_elem<MODE, 1>(a, acc[j], w[j], m[j], v[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < V; ++j) adam_elem<MODE, 0>(a, acc[j], w[j], m[j], v[j]);
     }
     store_floats<V>(a.w + i, w);
     if constexpr (uses_m(MODE)) store_floats<V>(a.m + i, m);
@@ -594,11 +614,13 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
                 for (int j = 0; j < E; ++j) {
                     gm[j] = finish_mean<PT>(acc[j], a);
                     if constexpr (MODE <= ZERO_MODE_FOLDED_STORAGE) // the only modes that divide
-                        special |= !(isfinite(gm[j]) && isfinite(m[j]) && isfinite(v[j]));
+                        special |= !(isfinite(gm[j]) && isfinite(m[j]) && isfinite(v[j])) || gm[j] == 0.0f;
                 }
-                // G = 2: the shortcuts for infinite operands are taken only by warps
-                // that hold a non-finite gradient mean or moment (one warp-uniform
-                // branch; both branches give the same IEEE results)
+                // G = 2: the shortcuts for infinite and zero operands are taken only
+                // by warps in which some lane holds a non-finite gradient mean or
+                // moment, or a zero gradient mean (what makes the numerators zero);
+                // one warp-uniform branch, and both branches give the same IEEE
+                // results
                 if (G == 1 || (G == 2 && __any_sync(__activemask(), special))) {
 #pragma unroll
                     for (int j = 0; j < E; ++j) adam_elem<MODE, 1>(a, gm[j], w[j], m[j], v[j]);
