@@ -544,3 +544,32 @@ def test_step_plan_names_the_kernel(z):
         assert plan == {"kernel": "bulk", "vector_width": 8, "ctas": 10}
     finally:
         z.zero_set_step_max_sms(prev)
+
+
+def test_untouched_embedding_rows(z):
+    """Rows of 768 parameters that no rank's batch touched: gradient exactly
+    zero on every rank (one row -0 on every rank) and moments still zero, so
+    whole warps take the branch that answers zero operands directly.  Four
+    steps on the bulk pipeline, whole arrays bit for bit."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    P, rows = 8, sms * 2048 * 4 // 768 + 3
+    N = rows * 768
+    stride = N
+    codes = synth.np_grads(P, N, stride, 1e-3, 71).reshape(P, rows, 768)
+    rng = np.random.default_rng(72)
+    untouched = rng.random(rows) < 0.3
+    codes[:, untouched, :] = 0
+    codes[:, np.flatnonzero(untouched)[0], :] = 0x8000          # -0 on every rank
+    codes = codes.reshape(-1)
+    w0, m0, v0, p0 = synth.np_state(N, 73)
+    ref = [w0.copy(), m0.copy(), v0.copy()]
+    s = dev_state(w0, m0, v0, p0)
+    g = dev_u16(codes)
+    _assert_path(z, "bulk", g, stride, s, N, P)
+    for t in range(1, 5):
+        gpu_step(z, g, stride, s, N, P, t, 0)
+        p_ref = oracle.adam_elems(codes, stride, P, *ref, t, LR, B1, B2, EPS, 0, threads=8)
+    assert max_ulps(host_state(s), ref + [p_ref]) == (0, 0)
+    # the untouched rows kept zero moments and their weights
+    m_now = host_state(s)[1].reshape(rows, 768)
+    assert not m_now[untouched].any()
