@@ -26,6 +26,7 @@ time ("scaling": "weak").
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -54,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="gpt2s",
                     choices=("tiny", "gpt2s", "tf1p3b", "shard7p5b", "folded"))
     ap.add_argument("--mode", type=int, default=None, help="Adam reading (default: the workload's first)")
+    ap.add_argument("--ranks", type=int, default=None,
+                    help="override the workload's rank count P (whole-vector workloads; N unchanged)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -805,6 +808,10 @@ def main(argv=None):
     args = parse_args(argv)
     from zero_sharded_mixed_shard_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
+    if args.ranks is not None:
+        if wl.shard is not None or not 1 <= args.ranks <= 1024:
+            raise SystemExit("--ranks takes 1..1024 on a whole-vector workload")
+        wl = dataclasses.replace(wl, P=args.ranks, name=f"{wl.name}-P{args.ranks}")
     mode = wl.modes[0] if args.mode is None else args.mode
     dist = Dist()
     if args.impl == "reference":

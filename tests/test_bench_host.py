@@ -82,3 +82,11 @@ def test_reference_arm_other_ranks_do_no_work(monkeypatch):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3"]) == 0
+
+
+def test_ranks_override_is_checked_before_any_gpu_work():
+    import bench
+    with pytest.raises(SystemExit):
+        bench.main(["--workload", "shard7p5b", "--ranks", "4"])
+    with pytest.raises(SystemExit):
+        bench.main(["--ranks", "0"])
