@@ -337,11 +337,12 @@ def _assert_path(z, kernel, g, stride, s, N, P, mode=0):
     assert plan["kernel"] == kernel, plan
 
 
-@pytest.mark.parametrize("P", [1, 2, 3, 4, 6, 8, 13, 16, 33, 64, 128, 256])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 6, 8, 13, 16, 33, 64, 72, 128, 144, 256])
 def test_tma_path_matches_oracle(z, P):
     """P that fills whole 8-rank chunks and P that leaves a partial last chunk;
-    every kind of instance (P = 1, 2, 4, 8, 16, 64, 128, 256 of their own;
-    3 on the generic one of 1024 consumers, 6, 13 and 33 on the one of 512);
+    every kind of instance (P = 1, 2, 4, 8, 16, 64, 72, 128, 144, 256 of their
+    own, 72 and 144 with a mean that is a true division; 3 on the generic
+    one of 1024 consumers, 6, 13 and 33 on the one of 512);
     a ragged tail of 5 elements; three steps of every mode."""
     N = _tma_size(4101)            # 4 x SMs full tiles, 2 more, a partial tile, a tail of 5
     stride = synth.round_up(N, 8) + 8

@@ -748,7 +748,9 @@ TmaKernel pick_tma_p(int P)
     case 16: return tma_instance<MODE, 16>();
     case 32: return tma_instance<MODE, 32>();
     case 64: return tma_instance<MODE, 64>();
+    case 72: return tma_instance<MODE, 72>();   // one NVL72 rack of GB300s
     case 128: return tma_instance<MODE, 128>();
+    case 144: return tma_instance<MODE, 144>(); // two racks
     case 256: return tma_instance<MODE, 256>();
     default: // measured: 256 consumers, as P = 8 takes, cost P = 5-7 20 %
         if (P <= 4) return tma_generic<MODE, tma_threads(4)>();
