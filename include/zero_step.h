@@ -452,6 +452,24 @@ int zero_mlp4_zero3_step_noalloc(const float* x, int32_t P, int32_t n, float* ma
  * ZERO_ECUDA. */
 int zero_device_timeouts(int64_t* count, int32_t reset);
 
+/* Diagnostic of the gradient mean for rank counts that are not powers of
+ * two (no counterpart on the pages).  The fused kernels form sum / P without
+ * a divide: with r = RN(1/P), q = RN(sum r), then q + RN(sum - q P) r by two
+ * fused multiply-adds (Markstein's correction step).  Whether that rounds to
+ * the correctly rounded quotient depends on P, so this call checks it on the
+ * current device against the correctly rounded divide for every P in
+ * [p_lo, p_hi] and every fp32 significand in [1, 2) -- 2^23 values per P,
+ * which covers every nonzero sum of P fp16 gradients, since those lie in
+ * [2^-24, 2^26] where scaling by a power of two scales each step exactly.
+ * *mismatches receives the number of (P, significand) pairs that differ
+ * (0 means the fast mean is the IEEE mean for those P); *first_p and
+ * *first_sum (each may be NULL) the first one found, or 0.  Synchronous
+ * (waits for its kernel on the legacy default stream); ~10 ms for all
+ * 1024 rank counts.  Errors: ZERO_EINVAL (mismatches NULL, p_lo < 1,
+ * p_hi < p_lo, p_hi > ZERO_MAX_RANKS), ZERO_ECUDA. */
+int zero_selftest_mean_division(int32_t p_lo, int32_t p_hi, int64_t* mismatches, int32_t* first_p,
+                                float* first_sum);
+
 /* Diagnostic of the bounded waits (no counterpart on the pages): enqueues
  * the step of zero_adam_step (same arguments) through the bulk-copy kernel
  * with one shared-memory barrier of its first CTA told to expect 16 bytes

@@ -167,3 +167,11 @@ def test_step_max_sms_setting(zlib):
         assert zlib.zero_set_step_max_sms(0) == 0
     finally:
         zlib.zero_set_step_max_sms(prev)
+
+
+def test_mean_division_check_rejects_bad_ranges(zlib):
+    """Host-side argument checks of the mean-division diagnostic (no CUDA call)."""
+    for lo, hi in ((0, 5), (5, 4), (1, zlib.ZERO_MAX_RANKS + 1)):
+        with pytest.raises(zlib.ZeroError) as e:
+            zlib.zero_selftest_mean_division(lo, hi)
+        assert e.value.code == zlib.ZERO_EINVAL

@@ -574,3 +574,13 @@ def test_untouched_embedding_rows(z):
     # the untouched rows kept zero moments and their weights
     m_now = host_state(s)[1].reshape(rows, 768)
     assert not m_now[untouched].any()
+
+
+def test_fast_mean_is_the_ieee_mean_for_every_rank_count(z):
+    """The divide-free mean (Markstein's correction step) equals the correctly
+    rounded sum / P for every fp32 significand and every P the library takes
+    (2^23 x 1024 cases, checked on the device against its correctly rounded
+    divide); by power-of-two scaling this covers every nonzero sum of fp16
+    gradients."""
+    n, p, s = z.zero_selftest_mean_division(1, z.ZERO_MAX_RANKS)
+    assert n == 0, f"{n} mismatches, the first at P = {p}, sum = {s!r}"

@@ -39,7 +39,7 @@ EXPORTED = ("zero_init_layout", "zero_free_layout", "zero_shard_range", "zero_me
             "zero_reduce_scatter_fp16", "zero_cpu_adam",
             "zero_offload_step", "zero_mlp4_loss", "zero_mlp4_layer_grads",
             "zero_mlp4_zero3_step", "zero_mlp4_zero3_step_noalloc", "zero_device_timeouts",
-            "zero_selftest_wait_timeout", "zero_strerror",
+            "zero_selftest_wait_timeout", "zero_selftest_mean_division", "zero_strerror",
             "zero_last_cuda_error", "zero_last_cuda_error_string")
 
 
@@ -143,6 +143,9 @@ def lib() -> ctypes.CDLL:
     L.zero_selftest_wait_timeout.argtypes = [vp, i64, vp, vp, vp, vp, i64, i32, i32, i64,
                                              f32, f32, f32, f32, i32, vp]
     L.zero_selftest_wait_timeout.restype = ctypes.c_int
+    L.zero_selftest_mean_division.argtypes = [i32, i32, ctypes.POINTER(ctypes.c_int64),
+                                              ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_float)]
+    L.zero_selftest_mean_division.restype = ctypes.c_int
     L.zero_device_timeouts.argtypes = [ctypes.POINTER(ctypes.c_int64), i32]
     L.zero_device_timeouts.restype = ctypes.c_int
     L.zero_strerror.argtypes = [ctypes.c_int]
@@ -271,6 +274,16 @@ def zero_step_plan(grads, rank_stride: int, master, m, v, params, N: int, P: int
         raise ZeroError(rc, "zero_step_plan")
     return {"kernel": "bulk" if k.value == ZERO_KERNEL_BULK else "vector",
             "vector_width": vw.value, "ctas": c.value}
+
+
+def zero_selftest_mean_division(p_lo: int, p_hi: int) -> tuple:
+    """(mismatches, first P, first sum) of the fast mean against the correctly
+    rounded divide for rank counts p_lo..p_hi (see include/zero_step.h)."""
+    n, fp, fs = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_float()
+    rc = lib().zero_selftest_mean_division(p_lo, p_hi, ctypes.byref(n), ctypes.byref(fp), ctypes.byref(fs))
+    if rc:
+        raise ZeroError(rc, "zero_selftest_mean_division")
+    return n.value, fp.value, fs.value
 
 
 def zero_device_timeouts(reset: bool = False) -> int:

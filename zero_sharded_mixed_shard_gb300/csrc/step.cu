@@ -59,7 +59,7 @@ struct StepArgs {
     long long head;     // leading elements processed one by one (alignment)
     int P;              // ranks
     int p_pow2;         // P is a power of two: g * (1/P) == g / P exactly
-    float inv_p;        // 1/P (exact when p_pow2)
+    float inv_p;        // RN(1/P), an IEEE division on the host (exact when p_pow2)
     float lr, b1, b2, omb1, omb2, bc1, bc2, bp1, bp2, eps;
     unsigned int poison_tx; // diagnostic only: extra bytes CTA 0's first barrier expects (0 otherwise)
 };
@@ -68,6 +68,23 @@ struct StepArgs {
 // Per-element arithmetic
 // ---------------------------------------------------------------------------
 
+// s / p correctly rounded without a divide, for finite nonzero s: with
+// r = RN(1/p), q = RN(s r) is within a few ulp of s / p, the remainder
+// s - q p is formed exactly by one fused multiply-add, and one correction
+// step q + (s - q p) r rounds to the quotient (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990).  That the last step rounds correctly is a property of p:
+// zero_selftest_mean_division checks it against the correctly rounded
+// divide for every fp32 significand and every p from 1 to 1024, which covers
+// every nonzero sum of fp16 gradients (they lie in [2^-24, 2^27), where
+// scaling s by a power of two scales every step exactly).
+__device__ __forceinline__ float div_by_count(float s, float p, float r)
+{
+    const float q = __fmul_rn(s, r);
+    const float e = __fmaf_rn(-q, p, s);
+    return __fmaf_rn(e, r, q);
+}
+
 template <int PT>
 __device__ __forceinline__ float finish_mean(float sum, const StepArgs& a)
 {
@@ -75,7 +92,9 @@ __device__ __forceinline__ float finish_mean(float sum, const StepArgs& a)
         return __fmul_rn(sum, 1.0f / static_cast<float>(PT));
     } else {
         if (a.p_pow2) return __fmul_rn(sum, a.inv_p);
-        return sum == 0.0f ? sum : __fdiv_rn(sum, static_cast<float>(a.P)); // +-0 / P = +-0
+        // +-0 / P = +-0, +-inf / P = +-inf, NaN stays NaN
+        return (sum == 0.0f || !isfinite(sum)) ? sum
+                                               : div_by_count(sum, static_cast<float>(PT > 0 ? PT : a.P), a.inv_p);
     }
 }
 
@@ -1301,6 +1320,60 @@ extern "C" int zero_device_timeouts(int64_t* count, int32_t reset)
         if (e != cudaSuccess) return record_cuda(e);
     }
     *count = n;
+    return ZERO_OK;
+}
+
+namespace {
+
+// Mismatches found by the mean-division check, and the first one's (p, s).
+__device__ unsigned long long g_div_mismatches;
+__device__ unsigned int g_div_first_p;
+__device__ float g_div_first_s;
+
+// div_by_count against the correctly rounded divide for every p in
+// [p_lo, p_hi] and every fp32 significand s in [1, 2); r is formed the way
+// the host forms StepArgs::inv_p, a correctly rounded 1/p.
+__global__ void zero_mean_division_check_kernel(int p_lo, int p_hi)
+{
+    const long long total = static_cast<long long>(p_hi - p_lo + 1) << 23;
+    const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long k = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; k < total; k += step) {
+        const int p = p_lo + static_cast<int>(k >> 23);
+        const float s = __uint_as_float(0x3f800000u | static_cast<unsigned int>(k & 0x7fffff));
+        const float pf = static_cast<float>(p);
+        const float want = __fdiv_rn(s, pf);
+        const float got = div_by_count(s, pf, __frcp_rn(pf));
+        if (__float_as_uint(want) != __float_as_uint(got) && atomicAdd(&g_div_mismatches, 1ull) == 0ull) {
+            g_div_first_p = static_cast<unsigned int>(p);
+            g_div_first_s = s;
+        }
+    }
+}
+
+} // namespace
+
+extern "C" int zero_selftest_mean_division(int32_t p_lo, int32_t p_hi, int64_t* mismatches, int32_t* first_p,
+                                           float* first_sum)
+{
+    if (!mismatches || p_lo < 1 || p_hi < p_lo || p_hi > ZERO_MAX_RANKS) return ZERO_EINVAL;
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return record_cuda(cudaGetLastError());
+    const unsigned long long zero = 0;
+    cudaError_t e = cudaMemcpyToSymbol(g_div_mismatches, &zero, sizeof(zero));
+    if (e != cudaSuccess) return record_cuda(e);
+    zero_mean_division_check_kernel<<<static_cast<unsigned int>(sms) * 8, kThreads>>>(p_lo, p_hi);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return record_cuda(e);
+    unsigned long long n = 0;
+    unsigned int fp = 0;
+    float fs = 0.0f;
+    e = cudaMemcpyFromSymbol(&n, g_div_mismatches, sizeof(n)); // waits for the kernel
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&fp, g_div_first_p, sizeof(fp));
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&fs, g_div_first_s, sizeof(fs));
+    if (e != cudaSuccess) return record_cuda(e);
+    *mismatches = static_cast<int64_t>(n);
+    if (first_p) *first_p = n ? static_cast<int32_t>(fp) : 0;
+    if (first_sum) *first_sum = n ? fs : 0.0f;
     return ZERO_OK;
 }
 
