@@ -360,9 +360,11 @@ int zero_cpu_adam(const void* grad_fp16, float* master, float* m, float* v, void
  * memory that the caller keeps alive, and leaves alone, until the stream has
  * passed this step.  The call returns at once.  Numerically the step differs
  * from zero_adam_step only in that the gradient mean is rounded to fp16 on
- * its way to the host.  Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ENOMEM (host
- * bookkeeping), ZERO_ECUDA (pieces enqueued before the failure stay
- * enqueued, and cuda_stream still waits for them when that is possible). */
+ * its way to the host.  Errors: ZERO_EINVAL (also for a current device
+ * numbered 64 or above, which has no slot for the internal streams),
+ * ZERO_EALIGN, ZERO_ENOMEM (host bookkeeping), ZERO_ECUDA (pieces enqueued
+ * before the failure stay enqueued, and cuda_stream still waits for them
+ * when that is possible). */
 int zero_offload_step(const void* grads_fp16, int64_t rank_stride, float* master_host, float* m_host,
                       float* v_host, void* grad16_host, void* params16_host, void* params_fp16,
                       int64_t N, int32_t P, int32_t stage, int64_t t, float lr, float beta1,
@@ -435,7 +437,8 @@ int zero_mlp4_zero3_step(const float* x, int32_t P, int32_t n, void* gathered_fp
  *    of the last call (each call writes every entry before reading it, so
  *    nothing needs clearing).  Calls whose work overlaps on the GPU -- on
  *    two streams, or from two host threads -- race on it: order them.
- * Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
+ * Errors: ZERO_EINVAL (also for a current device numbered 64 or above),
+ * ZERO_EALIGN, ZERO_ECUDA. */
 int zero_mlp4_zero3_step_noalloc(const float* x, int32_t P, int32_t n, float* master, float* m,
                                  float* v, void* shard_fp16, float* loss, int64_t t, float lr,
                                  float beta1, float beta2, float eps, int32_t mode,

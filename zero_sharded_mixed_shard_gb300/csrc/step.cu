@@ -816,14 +816,14 @@ int pick_vector(const StepArgs& a, int mode, long long* head)
 
 int sm_count_of_current_device()
 {
-    static std::atomic<int> cache[64];
+    static std::atomic<int> cache[64]; // devices 0..63; any other is asked every time
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev < 0 || dev >= 64) dev = 63;
-    int c = cache[dev].load(std::memory_order_relaxed);
+    const bool cached = dev >= 0 && dev < 64;
+    int c = cached ? cache[dev].load(std::memory_order_relaxed) : 0;
     if (c == 0) {
         if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cache[dev].store(c, std::memory_order_relaxed);
+        if (cached) cache[dev].store(c, std::memory_order_relaxed);
     }
     return c;
 }
@@ -836,14 +836,17 @@ int record_cuda(cudaError_t e)
 
 // Launch set-up done once per (kernel, device): the resident CTAs per SM of
 // a vector-path kernel, or the dynamic shared-memory opt-in of a bulk-path
-// kernel.  Returns the value (>= 1) or ZERO_ECUDA.
+// kernel.  Returns the value (>= 1) or ZERO_ECUDA.  The table has room for
+// every kernel of the library (about 120) on 8 devices; past that a kernel
+// is set up again on each launch, which is slower but gives the same result.
 struct SetupEntry {
     KernelFn fn;
     int dev;
     int value;
 };
+constexpr int kSetupEntries = 1024;
 std::mutex g_setup_mu;
-SetupEntry g_setup[256];
+SetupEntry g_setup[kSetupEntries];
 int g_setup_n = 0;
 
 int kernel_setup(KernelFn fn, bool bulk)
@@ -863,7 +866,7 @@ int kernel_setup(KernelFn fn, bool bulk)
         if (value < 1) value = 1;
     }
     if (e != cudaSuccess) return record_cuda(e);
-    if (g_setup_n < 256) g_setup[g_setup_n++] = SetupEntry{fn, dev, value};
+    if (g_setup_n < kSetupEntries) g_setup[g_setup_n++] = SetupEntry{fn, dev, value};
     return value;
 }
 
