@@ -59,15 +59,16 @@ def host_u16(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def run_workload(z, wl, mode, steps, check_steps):
+def run_workload(z, wl, mode, steps, check_steps, padded=True, kernel="bulk"):
     dev = "cuda"
     E, P = wl.elems, wl.P
-    stride = wl.rank_stride(True)
+    stride = wl.rank_stride(padded)
     g = torch.empty((P, stride), dtype=torch.float16, device=dev)
     master, m, v, params = synth.torch_state(E, wl.seed, dev, wl.master_sigma)
     # the full-size workloads run the bulk-copy pipeline, as in the benchmark
+    # (an unpadded rank stride puts the ranks off the 16-byte phase: vector kernel)
     plan = z.zero_step_plan(g, stride, master, m, v, params, E, P, wl.stage, mode)
-    assert plan["kernel"] == "bulk", (wl.name, plan)
+    assert plan["kernel"] == kernel, (wl.name, plan)
     wins = windows(wl, wl.seed)
     ref = {w: [master[w[0]:w[1]].cpu().numpy(), m[w[0]:w[1]].cpu().numpy(),
                v[w[0]:w[1]].cpu().numpy()] for w in wins}
@@ -140,6 +141,17 @@ def test_shard_of_7p5b_workload(z):
     wl = synth.WORKLOADS["shard7p5b"]
     assert wl.elems == 117_187_500 and wl.rank_stride(True) == 117_187_504
     worst, _ = run_workload(z, wl, 0, wl.steps, check_steps=set(range(1, wl.steps + 1)))
+    assert worst == (0, 0)
+    torch.cuda.empty_cache()
+
+
+def test_shard_of_7p5b_unpadded_layout(z):
+    """The packed receive buffer without padding: rank stride M = 117,187,500
+    (4 mod 8), so the ranks' rows sit on alternating 8-byte phases and the
+    step takes the vector kernel at width 4; two steps on sampled windows."""
+    wl = synth.WORKLOADS["shard7p5b"]
+    assert wl.rank_stride(False) == 117_187_500
+    worst, _ = run_workload(z, wl, 0, 2, check_steps={1, 2}, padded=False, kernel="vector")
     assert worst == (0, 0)
     torch.cuda.empty_cache()
 
