@@ -565,13 +565,20 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
         const uint32_t poison = (u == 0 && blockIdx.x == 0) ? a.poison_tx : 0u;
         mbar_arrive_expect_tx(&full[s], hb * rc + (c == 0 ? state_rows(MODE) * fb : 0) + poison);
         const __half* src = g0 + static_cast<long long>(c) * kChunkRanks * a.stride + i0;
-        for (int q = 0; q < rc; ++q)
-            bulk_load(st + static_cast<size_t>(q) * kTile * 2, src + q * a.stride, hb, &full[s], policy);
-        if (c == 0) {
+        // the larger group of rows first (measured: with few ranks the state
+        // rows first, P = 4 +2.5 %; with more, the gradient rows first).  Only
+        // where P is known at compile time: decided at run time, the generic
+        // instance lost 3-6 % (P = 3, 5)
+        const bool state_first = PT > 0 && c == 0 && state_rows(MODE) * 2 > rc;
+        auto load_state = [&]() {
             bulk_load(st + kGradBytes, w0 + i0, fb, &full[s], policy);
             if constexpr (uses_m(MODE)) bulk_load(st + kGradBytes + kTile * 4, m0 + i0, fb, &full[s], policy);
             if constexpr (uses_v(MODE)) bulk_load(st + kGradBytes + 2 * kTile * 4, v0 + i0, fb, &full[s], policy);
-        }
+        };
+        if (state_first) load_state();
+        for (int q = 0; q < rc; ++q)
+            bulk_load(st + static_cast<size_t>(q) * kTile * 2, src + q * a.stride, hb, &full[s], policy);
+        if (c == 0 && !state_first) load_state();
     };
 
     if (tid == 0)
