@@ -787,8 +787,8 @@ def run_mlp4(args, dist):
         for _ in range(reps):
             step()
         e1.record(main)
+        host_us = (time.perf_counter() - h0) * 1e6 / reps   # enqueueing only: before the wait
         torch.cuda.synchronize()
-        host_us = (time.perf_counter() - h0) * 1e6 / reps
         out["pipelined" if pipelined else "serial"] = {
             "us_per_step": e0.elapsed_time(e1) * 1e3 / reps, "host_enqueue_us_per_step": host_us,
             "loss_after_warmup": loss0, "loss_at_end": float(loss.mean())}
