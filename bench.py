@@ -206,9 +206,10 @@ def kernel_source_hash() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic(workload: str) -> float | None:
+def profiled_traffic(workload: str, kernel: str = "zero_fused_step_tma_kernel") -> float | None:
     """DRAM bytes per launch from the committed ncu summary of this workload,
-    if it was taken on the current kernel source."""
+    if it was taken on the current kernel source and of the kernel the step
+    launches now."""
     path = os.path.join(PROFILE_DIR, f"zero_fused_step_{workload}.txt")
     try:
         kv = {}
@@ -218,6 +219,8 @@ def profiled_traffic(workload: str) -> float | None:
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
         if kv.get("source_sha256") != kernel_source_hash():
+            return None
+        if not kv.get("kernel", "").startswith(kernel.split(" ")[0]):
             return None
         return float(kv["traffic_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -414,7 +417,7 @@ def run_ours(args, wl, mode, dist):
                          f"{len(times)} consecutive steps in {sum(times):.1f} s"}
 
     if dist.rank == 0:
-        traffic = profiled_traffic(wl.name) if plan["kernel"] == "bulk" else None
+        traffic = profiled_traffic(wl.name, kernel_name)
         line = {
             "metric": "params updated/sec and achieved HBM GB/s (% of GB300 peak) per Adam step",
             "value": value, "unit": "params/s", "n_gpus": dist.world, "steps": K,

@@ -35,14 +35,17 @@ def test_clock_parser_keeps_samples_of_the_timed_region():
     assert c["reasons"] == ["sw_power_cap"]
 
 
-def test_profile_traffic_requires_matching_source(tmp_path, monkeypatch):
+def test_profile_traffic_requires_matching_source_and_kernel(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "PROFILE_DIR", str(tmp_path))
     f = tmp_path / "zero_fused_step_gpt2s.txt"
-    f.write_text(f"source_sha256: {bench.kernel_source_hash()}\ntraffic_bytes_per_launch: 123\n")
+    head = "kernel: zero_fused_step_tma_kernel<0,8,256,2>\n"
+    f.write_text(head + f"source_sha256: {bench.kernel_source_hash()}\ntraffic_bytes_per_launch: 123\n")
     assert bench.profiled_traffic("gpt2s") == 123.0
-    f.write_text("source_sha256: 0000\ntraffic_bytes_per_launch: 123\n")
+    # a summary of the other kernel does not describe this launch
+    assert bench.profiled_traffic("gpt2s", "zero_fused_step_kernel (vector width 8)") is None
+    f.write_text(head + "source_sha256: 0000\ntraffic_bytes_per_launch: 123\n")
     assert bench.profiled_traffic("gpt2s") is None
-    assert bench.profiled_traffic("tiny") is None
+    assert bench.profiled_traffic("shard7p5b") is None
 
 
 def _free_port():
