@@ -32,8 +32,13 @@
  *  - Return 0 (ZERO_OK) on success or a negative ZERO_E* code; the code's
  *    text is zero_strerror(code).  A rejected call has no side effects.
  *  - Device pointers are caller-owned (for example torch tensors).  The
- *    library never allocates, frees or synchronises device memory; kernels
- *    are enqueued on the caller's stream and the call returns immediately.
+ *    library never allocates or frees device memory; kernels are enqueued
+ *    on the caller's stream and the call returns immediately.  The only
+ *    calls that wait for the device are the two diagnostics that read a
+ *    device counter back (zero_device_timeouts, zero_selftest_mean_division);
+ *    zero_cpu_adam runs on the calling host thread.  The offload step
+ *    keeps two internal streams per device and the host Adam a pool of
+ *    host threads, both created on first use and kept.
  *  - Element counts and strides are in elements, not bytes.
  *  - fp16 buffers are passed as void* holding IEEE binary16 codes.
  *  - zero_adam_step, zero_adam_step_shard and zero_adam_step_range enqueue
