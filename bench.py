@@ -57,6 +57,9 @@ def parse_args(argv=None):
     ap.add_argument("--mode", type=int, default=None, help="Adam reading (default: the workload's first)")
     ap.add_argument("--ranks", type=int, default=None,
                     help="override the workload's rank count P (whole-vector workloads; N unchanged)")
+    ap.add_argument("--elements", type=int, default=None,
+                    help="override the workload's element count N (whole-vector workloads; a smaller case "
+                         "of the same kernel, e.g. for a profiler capture)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -815,6 +818,10 @@ def main(argv=None):
         if wl.shard is not None or not 1 <= args.ranks <= 1024:
             raise SystemExit("--ranks takes 1..1024 on a whole-vector workload")
         wl = dataclasses.replace(wl, P=args.ranks, name=f"{wl.name}-P{args.ranks}")
+    if args.elements is not None:
+        if wl.shard is not None or args.elements < 1:
+            raise SystemExit("--elements takes N >= 1 on a whole-vector workload")
+        wl = dataclasses.replace(wl, N=args.elements, tensors=None, name=f"{wl.name}-N{args.elements}")
     mode = wl.modes[0] if args.mode is None else args.mode
     dist = Dist()
     if args.impl == "reference":

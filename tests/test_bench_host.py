@@ -93,3 +93,7 @@ def test_ranks_override_is_checked_before_any_gpu_work():
         bench.main(["--workload", "shard7p5b", "--ranks", "4"])
     with pytest.raises(SystemExit):
         bench.main(["--ranks", "0"])
+    with pytest.raises(SystemExit):
+        bench.main(["--workload", "shard7p5b", "--elements", "1000"])
+    with pytest.raises(SystemExit):
+        bench.main(["--elements", "0"])
