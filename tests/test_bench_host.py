@@ -3,6 +3,7 @@ parser, the profile lookup, and the multi-process path (barrier and the
 max over ranks) as two gloo ranks on CPU."""
 import os
 import socket
+import subprocess
 import sys
 import time
 
@@ -97,3 +98,26 @@ def test_ranks_override_is_checked_before_any_gpu_work():
         bench.main(["--workload", "shard7p5b", "--elements", "1000"])
     with pytest.raises(SystemExit):
         bench.main(["--elements", "0"])
+
+
+def test_reference_arm_prints_one_contract_line():
+    """bench.py --impl reference (the CPU oracle on the host cores) prints one
+    JSON line with every key the benchmark contract asks for."""
+    import json
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "tiny", "--steps", "2", "--warmup", "3"], capture_output=True, text=True, timeout=600,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["value"] > 0 and d["higher_is_better"] is True and "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
