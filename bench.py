@@ -824,6 +824,9 @@ def main(argv=None):
         wl = dataclasses.replace(wl, N=args.elements, tensors=None, name=f"{wl.name}-N{args.elements}")
     mode = wl.modes[0] if args.mode is None else args.mode
     dist = Dist()
+    if args.gpus != dist.world:
+        raise SystemExit(f"--gpus {args.gpus} but {dist.world} process(es): launch N > 1 as "
+                         f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py --gpus {args.gpus}")
     if args.impl == "reference":
         return run_reference(args, wl, mode, dist)
     if args.overlap:

@@ -85,7 +85,7 @@ def test_two_gloo_ranks_take_the_slowest_time():
 def test_reference_arm_other_ranks_do_no_work(monkeypatch):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
-    assert bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3"]) == 0
+    assert bench.main(["--impl", "reference", "--gpus", "2", "--steps", "3", "--warmup", "3"]) == 0
 
 
 def test_ranks_override_is_checked_before_any_gpu_work():
@@ -98,6 +98,8 @@ def test_ranks_override_is_checked_before_any_gpu_work():
         bench.main(["--workload", "shard7p5b", "--elements", "1000"])
     with pytest.raises(SystemExit):
         bench.main(["--elements", "0"])
+    with pytest.raises(SystemExit):        # two GPUs asked for, one process running
+        bench.main(["--gpus", "2", "--impl", "reference"])
 
 
 def test_reference_arm_prints_one_contract_line():
