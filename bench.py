@@ -4,16 +4,20 @@
 One step = one call of ``zero_adam_step`` (all P simulated ranks' shards:
 reduce-scatter of the fp16 gradients, fp32 Adam, fp16 cast, write into the
 gathered parameter vector) over one batch of synthetic gradients.  The
-default workload is the GPT-2-small sized flat vector: N = 124,439,808
-parameters, P = 8 ranks, ZeRO-1, standard Adam, gradients ~ N(0, 1e-3) with
-1 % of entries x100.
+default workload is the largest that fits one GPU: N = 1.3e9 parameters laid
+out as 24 transformer blocks at d = 2048 plus an embedding, P = 16 ranks,
+ZeRO-2, standard Adam, gradients ~ N(0, 1e-4).
 
 Printed: one JSON line (rank 0).  ``value`` is parameters updated per second
 over the whole job with every input resident in HBM; ``e2e`` is the same
 metric with each step's gradients copied from pinned host memory and the
 gathered fp16 parameters copied back inside the timed region;
 ``roofline`` rates the fused kernel against the measured HBM copy bandwidth;
-``cpu_baseline`` times the CPU oracle on a bounded sample on the host cores.
+``per_config`` times every other workload (the 1,000,003-element vector, the
+GPT-2-small vector, one shard of a 7.5e9 model at P = 64 and both folded Adam
+readings at P = 32) in the same run, each with its own roofline fraction;
+``cpu_baseline`` times the CPU oracle on the host cores, single-threaded and
+on every core the process may use, on bounded samples of every workload.
 
 ``--impl reference`` times the CPU oracle instead (the only other
 implementation of this step), on the same workload and metric.
@@ -40,8 +44,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 NOMINAL_HBM_GBS = 8000.0
-L2_FALLBACK_BYTES = 129 * 1024 * 1024   # GB300's L2, when the device properties lack it
+L2_BYTES = 129 * 1024 * 1024   # GB300's L2 (nominal)
 DEFAULT_STEPS = {"tiny": 20000, "gpt2s": 2500, "tf1p3b": 200, "shard7p5b": 800, "folded": 600}
+# every workload with each Adam reading it runs; the headline is one of them,
+# the rest go to the line's per_config block
+ALL_CONFIGS = (("tiny", 0), ("gpt2s", 0), ("tf1p3b", 0), ("shard7p5b", 0), ("folded", 1), ("folded", 2))
+# timed steps of a per_config leg: at least this many (about 0.2 s of GPU time)
+PER_CONFIG_MIN_STEPS = {"tiny": 2000, "gpt2s": 250, "tf1p3b": 20, "shard7p5b": 80, "folded": 60}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SRC = os.path.join(ROOT, "zero_sharded_mixed_shard_gb300", "csrc", "step.cu")
 
@@ -52,7 +61,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="gpt2s",
+    ap.add_argument("--workload", default="tf1p3b",
                     choices=("tiny", "gpt2s", "tf1p3b", "shard7p5b", "folded"))
     ap.add_argument("--mode", type=int, default=None, help="Adam reading (default: the workload's first)")
     ap.add_argument("--ranks", type=int, default=None,
@@ -61,9 +70,11 @@ def parse_args(argv=None):
                     help="override the workload's element count N (whole-vector workloads; a smaller case "
                          "of the same kernel, e.g. for a profiler capture)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time the chosen workload only (no per_config block)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0,
-                    help="wall time budget of the CPU-oracle leg")
+    ap.add_argument("--cpu-seconds", type=float, default=24.0,
+                    help="wall time budget of the CPU-oracle leg (all of its runs together)")
     ap.add_argument("--overlap", action="store_true",
                     help="time the bucketed step overlapped with a synthetic backward instead")
     ap.add_argument("--bucket-elems", type=int, default=1 << 24)
@@ -132,7 +143,7 @@ CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event
 
 
 class ClockSampler:
-    def __init__(self, gpu_index: int, period_ms: int = 100):
+    def __init__(self, gpu_index: int, period_ms: int = 50):
         self.proc = None
         self.out = None
         self.gpu = gpu_index
@@ -150,10 +161,11 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.3)
 
-    def stop(self, t0: float, t1: float) -> dict:
+    def stop(self, *windows) -> list:
+        """Stop sampling; for each (t0, t1) host-time window, the clocks seen in it."""
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "nvidia-smi unavailable"}
+            return [{"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                     "note": "nvidia-smi unavailable"} for _ in windows]
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -164,7 +176,7 @@ class ClockSampler:
         text = self.out.read()
         self.out.close()
         os.unlink(self.out.name)
-        return parse_clock_csv(text, t0, t1)
+        return [parse_clock_csv(text, t0, t1) for t0, t1 in windows]
 
 
 def parse_clock_csv(text: str, t0: float, t1: float) -> dict:
@@ -234,21 +246,53 @@ def profiled_traffic(workload: str, kernel: str = "zero_fused_step_tma_kernel") 
 # the CPU oracle leg (used by cpu_baseline and by --impl reference)
 # ---------------------------------------------------------------------------
 
-def oracle_rate(wl, mode: int, budget_s: float, sample: int | None = None, steps: int | None = None):
-    """Time the oracle (as it stands, all host cores) on the first ``sample``
-    elements of the workload, all P ranks.  Returns (params/s, cores, sample,
+def host_cores() -> tuple[int, int]:
+    """(logical CPUs of the machine -- what std::thread::hardware_concurrency
+    reports --, CPUs this process may run on, from its affinity mask)."""
+    hw = os.cpu_count() or 1
+    try:
+        allowed = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        allowed = hw
+    return hw, allowed
+
+
+def oracle_inputs(wl, sample: int, draw: int | None = None):
+    """Seeded host inputs for ``sample`` elements of the workload, all P
+    ranks.  With ``draw`` < sample, a draw of that many elements is repeated
+    to fill the sample (the oracle's time does not depend on the values
+    beyond their mix, which the repeated draw keeps)."""
+    import numpy as np
+
+    from zero_sharded_mixed_shard_gb300 import synth
+    n = sample if draw is None else min(draw, sample)
+    codes = synth.np_grads(wl.P, n, n, wl.grad_sigma, wl.seed, wl.heavy_tail_frac, wl.zero_frac)
+    w, m, v, _ = synth.np_state(n, wl.seed, wl.master_sigma)
+    if n < sample:
+        reps = -(-sample // n)
+        codes = np.ascontiguousarray(np.tile(codes.reshape(wl.P, n), (1, reps))[:, :sample]).reshape(-1)
+        w = np.ascontiguousarray(np.tile(w, reps)[:sample])
+        m = np.zeros(sample, np.float32)
+        v = np.zeros(sample, np.float32)
+    return codes, w, m, v
+
+
+def oracle_rate(wl, mode: int, budget_s: float, sample: int | None = None, steps: int | None = None,
+                threads: int | None = None, draw: int | None = None):
+    """Time the oracle (as it stands) on the first ``sample`` elements of
+    the workload, all P ranks, ``threads`` host threads (default: every CPU
+    the process may use), consecutive steps until ``budget_s`` has passed
+    (at least one) or ``steps`` steps.  Returns (params/s, threads, sample,
     per-step seconds list)."""
     import numpy as np
 
     import oracle
-    from zero_sharded_mixed_shard_gb300 import synth
     oracle.build()
-    cores = os.cpu_count() or 1
+    if threads is None:
+        threads = host_cores()[1]
     if sample is None:
         sample = min(wl.elems, 1 << 24)
-    codes = synth.np_grads(wl.P, sample, sample, wl.grad_sigma, wl.seed,
-                           wl.heavy_tail_frac, wl.zero_frac)
-    w, m, v, _ = synth.np_state(sample, wl.seed, wl.master_sigma)
+    codes, w, m, v = oracle_inputs(wl, sample, draw)
     out = np.empty(sample, np.uint16)
     times = []
     t = 0
@@ -257,14 +301,53 @@ def oracle_rate(wl, mode: int, budget_s: float, sample: int | None = None, steps
         t += 1
         t0 = time.perf_counter()
         oracle.adam_elems(codes, sample, wl.P, w, m, v, t, wl.lr, wl.b1, wl.b2, wl.eps, mode,
-                          threads=cores, params_out=out)
+                          threads=threads, params_out=out)
         times.append(time.perf_counter() - t0)
         if steps is not None:
             if t >= steps:
                 break
         elif time.perf_counter() - start >= budget_s:
             break
-    return sample * len(times) / sum(times), cores, sample, times
+    return sample * len(times) / sum(times), threads, sample, times
+
+
+def cpu_baseline_leg(wl, mode: int, budget_s: float, configs=()) -> dict:
+    """The oracle on the host cores: the headline workload on every allowed
+    CPU and on one thread, and a per-element rate for each other workload.
+    The tiny and GPT-2-small workloads are timed on whole steps; the larger
+    ones on their first 2^22 elements, extrapolated to a whole step and
+    labelled so (elements never interact, so the per-element cost is the
+    same everywhere in the vector)."""
+    from zero_sharded_mixed_shard_gb300 import synth
+    hw, allowed = host_cores()
+    rate, threads, sample, times = oracle_rate(wl, mode, 0.35 * budget_s)
+    one_sample = min(wl.elems, 1 << 22)
+    rate1, _, _, times1 = oracle_rate(wl, mode, 0.2 * budget_s, sample=one_sample, threads=1)
+    out = {"value": rate, "unit": "params/s", "cores": threads, "kind": "oracle",
+           "sample": f"elements [0, {sample}) of the {wl.name} workload, all {wl.P} ranks, "
+                     f"{len(times)} consecutive steps in {sum(times):.1f} s on {threads} threads",
+           "hardware_concurrency": hw, "affinity_cores": allowed, "threads_used": threads,
+           "single_thread": {"value": rate1, "unit": "params/s", "threads_used": 1,
+                             "sample": f"elements [0, {one_sample}) of the {wl.name} workload, "
+                                       f"{len(times1)} steps in {sum(times1):.1f} s"},
+           "full_step_s_extrapolated": wl.elems / rate}
+    per = {}
+    share = 0.45 * budget_s / max(1, len(configs))
+    for cwl, cmode in configs:
+        whole = cwl.elems * cwl.P <= (1 << 30)    # tiny and gpt2s: whole steps
+        n = cwl.elems if whole else min(cwl.elems, 1 << 22)
+        r, th, n, ts = oracle_rate(cwl, cmode, share, sample=n, draw=min(n, 1 << 22))
+        per[f"{cwl.name}/mode{cmode}"] = {
+            "value": r, "unit": "params/s", "threads_used": th,
+            "gbs": r * synth.bytes_per_elem(cwl.P, cmode) / 1e9,
+            "kind": "whole step" if whole else "elements [0, 2^22), extrapolated to a whole step",
+            "sample": (f"all {n} elements" if whole else f"elements [0, {n})")
+                      + f", {len(ts)} steps in {sum(ts):.1f} s"
+                      + (" (a 2^22-element draw repeated to fill the vector)" if whole and n > (1 << 22) else ""),
+            "step_s": cwl.elems / r}
+    if per:
+        out["per_config"] = per
+    return out
 
 
 def run_reference(args, wl, mode, dist):
@@ -281,17 +364,21 @@ def run_reference(args, wl, mode, dist):
     timed = times[args.warmup:]
     sec = sum(timed)
     value = sample * len(timed) / sec
+    hw, allowed = host_cores()
+    note = (f"each step runs the oracle on elements [0, {sample}) of the {wl.name} workload, all "
+            f"{wl.P} ranks; params/s counts those elements")
     line = {
         "impl": "reference",
         "metric": "params updated/sec and achieved HBM GB/s (% of GB300 peak) per Adam step",
         "value": value, "unit": "params/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(timed), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(wl, mode, sample_note=f"first {sample} elements per step"),
+        "config": workload_config(wl, mode, l2_flush_bytes=l2_flush_for(wl, mode)),
+        "sample": note,
         "achieved_gbs": value * synth.bytes_per_elem(wl.P, mode) / 1e9,
         "cpu_baseline": {"value": value, "unit": "params/s", "cores": cores, "kind": "oracle",
-                         "sample": f"elements [0, {sample}) of the {wl.name} workload, all "
-                                   f"{wl.P} ranks, one oracle call per step"},
+                         "sample": note, "hardware_concurrency": hw, "affinity_cores": allowed,
+                         "threads_used": cores},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -299,7 +386,17 @@ def run_reference(args, wl, mode, dist):
     return 0
 
 
-def workload_config(wl, mode, sample_note=None, l2_flush_bytes=None):
+def l2_flush_for(wl, mode) -> int | None:
+    """Bytes written between timed steps to flush L2, or None: a step that
+    moves less than twice the L2 would partly run from L2 when repeated, so
+    a buffer of 4x the L2 is written between its timed steps and only the
+    steps themselves are timed."""
+    from zero_sharded_mixed_shard_gb300 import synth
+    alg = wl.elems * synth.bytes_per_elem(wl.P, mode)
+    return 4 * L2_BYTES if alg < 2 * L2_BYTES else None
+
+
+def workload_config(wl, mode, l2_flush_bytes=None):
     from zero_sharded_mixed_shard_gb300 import synth
     step_gb = wl.elems * synth.bytes_per_elem(wl.P, mode) / 1e9
     if l2_flush_bytes:
@@ -313,14 +410,92 @@ def workload_config(wl, mode, sample_note=None, l2_flush_bytes=None):
            "N": wl.N, "elements_per_step": wl.elems, "P": wl.P, "stage": wl.stage, "mode": mode,
            "rank_stride": wl.rank_stride(True), "bytes_per_elem": synth.bytes_per_elem(wl.P, mode),
            "l2": l2}
-    if sample_note:
-        cfg["sample"] = sample_note
     return cfg
 
 
-# ---------------------------------------------------------------------------
-# our arm
-# ---------------------------------------------------------------------------
+def kernel_label(plan) -> str:
+    return ("zero_fused_step_tma_kernel" if plan["kernel"] == "bulk"
+            else f"zero_fused_step_kernel (vector width {plan['vector_width']})")
+
+
+class Timed:
+    """One workload on the device: its buffers, a step function and the
+    timing of K steps after W warm-up steps (CUDA events on the launching
+    stream, one pair per step)."""
+
+    def __init__(self, z, wl, mode, dist, device, stream):
+        import torch
+
+        from zero_sharded_mixed_shard_gb300 import synth
+        self.z, self.wl, self.mode, self.dist, self.stream = z, wl, mode, dist, stream
+        E, P = wl.elems, wl.P
+        self.stride = wl.rank_stride(True)
+        self.g = synth.torch_grads(P, E, self.stride, wl.grad_sigma, wl.seed + 17 * dist.rank, device,
+                                   wl.heavy_tail_frac, wl.zero_frac, step=1)
+        self.master, self.m, self.v, self.params = synth.torch_state(E, wl.seed + 17 * dist.rank, device,
+                                                                     wl.master_sigma)
+        # the kernel the step launches (the shard call is a step of E elements
+        # from the same buffers, so it takes the same decision)
+        self.plan = z.zero_step_plan(self.g, self.stride, self.master, self.m, self.v, self.params, E, P,
+                                     wl.stage, mode)
+        self.alg_bytes = E * synth.bytes_per_elem(P, mode)
+        fb = l2_flush_for(wl, mode)
+        self.flush = torch.empty(fb, dtype=torch.uint8, device=device) if fb else None
+        self.t = 0
+
+    def step(self, g=None):
+        wl, z = self.wl, self.z
+        self.t += 1
+        g = self.g if g is None else g
+        if wl.shard is None:
+            z.zero_adam_step(g, self.stride, self.master, self.m, self.v, self.params, wl.N, wl.P,
+                             wl.stage, self.t, wl.lr, wl.b1, wl.b2, wl.eps, self.mode, self.stream)
+        else:
+            z.zero_adam_step_shard(g, self.stride, 0, wl.shard, self.master, self.m, self.v,
+                                   self.params, wl.N, wl.P, wl.stage, self.t, wl.lr, wl.b1, wl.b2,
+                                   wl.eps, self.mode, self.stream)
+
+    def warm(self, W):
+        import torch
+        for _ in range(W):
+            if self.flush is not None:
+                self.flush.zero_()
+            self.step()
+        torch.cuda.synchronize()
+
+    def run(self, K):
+        """Time K steps (the caller brackets them with barrier + synchronize).
+        Returns (region ms, mean launch ms); with an L2 flush between steps
+        the region is the sum of the steps' own times."""
+        import torch
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        for i in range(K):
+            if self.flush is not None:
+                self.flush.zero_()
+            starts[i].record(self.stream)
+            self.step()
+            ends[i].record(self.stream)
+        torch.cuda.synchronize()
+        launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        region_ms = starts[0].elapsed_time(ends[-1]) if self.flush is None else sum(launch_ms)
+        return region_ms, sum(launch_ms) / K
+
+    def free(self):
+        import torch
+        self.g = self.master = self.m = self.v = self.params = self.flush = None
+        torch.cuda.empty_cache()
+
+
+def roofline_entry(wl, mode, plan, alg_bytes, mean_launch_ms):
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (mean_launch_ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": profiled_traffic(wl.name, kernel_label(plan)),
+            "kernel": kernel_label(plan), "ctas": plan["ctas"],
+            "peak_kind": f"{peak_kind} HBM copy bandwidth",
+            "algorithmic_bytes_per_launch": alg_bytes, "mean_launch_ms": mean_launch_ms}
+
 
 def run_ours(args, wl, mode, dist):
     import torch
@@ -334,93 +509,72 @@ def run_ours(args, wl, mode, dist):
     dist.init("nccl")
     device = torch.device("cuda", dist.local_rank)
     z.lib()
-
-    E, P = wl.elems, wl.P
-    stride = wl.rank_stride(True)
-    g = synth.torch_grads(P, E, stride, wl.grad_sigma, wl.seed + 17 * dist.rank, device,
-                          wl.heavy_tail_frac, wl.zero_frac, step=1)
-    master, m, v, params = synth.torch_state(E, wl.seed + 17 * dist.rank, device, wl.master_sigma)
     stream = torch.cuda.current_stream(device)
 
-    def step(t):
-        if wl.shard is None:
-            z.zero_adam_step(g, stride, master, m, v, params, wl.N, P, wl.stage, t, wl.lr,
-                             wl.b1, wl.b2, wl.eps, mode, stream)
-        else:
-            z.zero_adam_step_shard(g, stride, 0, wl.shard, master, m, v, params, wl.N, P,
-                                   wl.stage, t, wl.lr, wl.b1, wl.b2, wl.eps, mode, stream)
-
-    # the kernel the step launches (the shard call is a step of E elements
-    # from the same buffers, so it takes the same decision)
-    plan = z.zero_step_plan(g, stride, master, m, v, params, E, P, wl.stage, mode)
-    kernel_name = ("zero_fused_step_tma_kernel" if plan["kernel"] == "bulk"
-                   else f"zero_fused_step_kernel (vector width {plan['vector_width']})")
-
-    # A step that moves less than twice the L2 would partly run from L2 when
-    # repeated: then a buffer larger than L2 is written between timed steps,
-    # only the steps themselves are timed, and the throughput comes from
-    # their summed durations.
-    alg_bytes = E * synth.bytes_per_elem(P, mode)
-    l2_bytes = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or L2_FALLBACK_BYTES
-    flush = None
-    if alg_bytes < 2 * l2_bytes:
-        flush = torch.empty(4 * l2_bytes, dtype=torch.uint8, device=device)
-
-    t = 0
-    for _ in range(args.warmup):
-        t += 1
-        if flush is not None:
-            flush.zero_()
-        step(t)
-    torch.cuda.synchronize()
-
+    head = Timed(z, wl, mode, dist, device, stream)
+    head.warm(args.warmup)
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     sampler = ClockSampler(dist.local_rank)
     if dist.rank == 0:
         sampler.start()
     dist.barrier()
     torch.cuda.synchronize()
     h0 = time.time()
-    for i in range(K):
-        t += 1
-        if flush is not None:
-            flush.zero_()
-        starts[i].record(stream)
-        step(t)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    region_ms, mean_launch_ms = head.run(K)
     h1 = time.time()
     dist.barrier()
-    clocks = sampler.stop(h0, h1) if dist.rank == 0 else None
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    region_ms = starts[0].elapsed_time(ends[-1]) if flush is None else sum(launch_ms)
     region_ms = dist.max(region_ms, device)
-    mean_launch_ms = dist.max(sum(launch_ms) / K, device)
-
-    elems_total = E * K * dist.world
-    value = elems_total / (region_ms / 1e3)
-    achieved = alg_bytes / (mean_launch_ms / 1e3) / 1e9
-    peak, peak_kind = measured_peaks()
+    mean_launch_ms = dist.max(mean_launch_ms, device)
+    E = wl.elems
+    value = E * K * dist.world / (region_ms / 1e3)
 
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(z, wl, mode, g, master, m, v, params, stride, stream, device, dist, t,
-                      K_e2e=max(3, min(K, 100)))
+        e2e = run_e2e(head, device, dist)
+    flush_bytes = None if head.flush is None else head.flush.numel()
+    plan, alg_bytes = head.plan, head.alg_bytes
+    head.free()
+    del head
 
-    del g
-    torch.cuda.empty_cache()
+    # every other workload, in the same run and under the same clock sampler
+    per_config = None
+    p0 = p1 = None
+    if not args.no_per_config and args.ranks is None and args.elements is None:
+        per_config = {}
+        p0 = time.time()
+        for name, cmode in ALL_CONFIGS:
+            if (name, cmode) == (wl.name, mode):
+                continue
+            cwl = synth.WORKLOADS[name]
+            leg = Timed(z, cwl, cmode, dist, device, stream)
+            leg.warm(args.warmup)
+            ck = max(K, PER_CONFIG_MIN_STEPS[name])
+            dist.barrier()
+            torch.cuda.synchronize()
+            r_ms, l_ms = leg.run(ck)
+            dist.barrier()
+            r_ms, l_ms = dist.max(r_ms, device), dist.max(l_ms, device)
+            per_config[f"{name}/mode{cmode}"] = {
+                "workload": workload_config(cwl, cmode, None if leg.flush is None else leg.flush.numel())["workload"],
+                "value": cwl.elems * ck * dist.world / (r_ms / 1e3), "unit": "params/s", "steps": ck,
+                "ms_per_step": r_ms / ck,
+                "roofline": roofline_entry(cwl, cmode, leg.plan, leg.alg_bytes, l_ms),
+                "l2": "flushed between timed steps" if leg.flush is not None else "inputs larger than L2"}
+            leg.free()
+            del leg
+        p1 = time.time()
+    clocks_list = sampler.stop((h0, h1), *([(p0, p1)] if p0 is not None else [])) if dist.rank == 0 else None
+    if per_config is not None and clocks_list:
+        per_config["clocks"] = clocks_list[1] if len(clocks_list) > 1 else None
+
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        rate, cores, sample, times = oracle_rate(wl, mode, args.cpu_seconds)
-        cpu = {"value": rate, "unit": "params/s", "cores": cores, "kind": "oracle",
-               "sample": f"elements [0, {sample}) of the {wl.name} workload, all {P} ranks, "
-                         f"{len(times)} consecutive steps in {sum(times):.1f} s"}
+        others = [] if per_config is None else [
+            (synth.WORKLOADS[n], cm) for n, cm in ALL_CONFIGS if (n, cm) != (wl.name, mode)]
+        cpu = cpu_baseline_leg(wl, mode, args.cpu_seconds, others)
 
     if dist.rank == 0:
-        traffic = profiled_traffic(wl.name, kernel_name)
         line = {
             "metric": "params updated/sec and achieved HBM GB/s (% of GB300 peak) per Adam step",
             "value": value, "unit": "params/s", "n_gpus": dist.world, "steps": K,
@@ -428,18 +582,14 @@ def run_ours(args, wl, mode, dist):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "io_dtypes": "fp16 gradients and parameters, fp32 master/m/v",
             "data": "synthetic (seeded device RNG)",
-            "config": workload_config(wl, mode, l2_flush_bytes=None if flush is None else flush.numel()),
+            "config": workload_config(wl, mode, l2_flush_bytes=flush_bytes),
             "achieved_hbm_gbs": alg_bytes * K * dist.world / (region_ms / 1e3) / 1e9,
             "pct_of_nominal_8tbs": 100 * alg_bytes * K / (region_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "kernel": kernel_name, "ctas": plan["ctas"],
-                         "peak_kind": f"{peak_kind} HBM copy bandwidth",
-                         "algorithmic_bytes_per_launch": alg_bytes,
-                         "mean_launch_ms": mean_launch_ms},
+            "roofline": roofline_entry(wl, mode, plan, alg_bytes, mean_launch_ms),
             "gpu_launches": K,
-            "clocks": clocks,
+            "clocks": clocks_list[0] if clocks_list else None,
             "e2e": e2e,
+            "per_config": per_config,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -447,7 +597,7 @@ def run_ours(args, wl, mode, dist):
     return 0
 
 
-def run_e2e(z, wl, mode, g, master, m, v, params, stride, stream, device, dist, t, K_e2e):
+def run_e2e(head, device, dist):
     """Each step: pinned host gradients -> device, the step, gathered fp16
     parameters -> pinned host; all inside the timed region.
 
@@ -455,11 +605,19 @@ def run_e2e(z, wl, mode, g, master, m, v, params, stride, stream, device, dist, 
     k+1's gradients (into the second of two device buffers, on its own
     stream) runs while step k's kernel and the download of its parameters
     run; step k+1's kernel waits for its upload and for the download of
-    step k's parameters (which it overwrites)."""
+    step k's parameters (which it overwrites).  The number of steps is
+    bounded so the leg takes about 5 s (the upload is limited by the host
+    link, ~200 GB/s)."""
     import torch
-    host_g = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+    g, params, stream = head.g, head.params, head.stream
+    try:
+        host_g = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+        host_p = torch.empty(params.shape, dtype=params.dtype, pin_memory=True)
+    except RuntimeError as exc:   # the host could not page-lock that much memory
+        return {"value": None, "unit": "params/s", "unavailable": f"pinned host buffers: {exc}"[:200]}
     host_g.copy_(g)
-    host_p = torch.empty(params.shape, dtype=params.dtype, pin_memory=True)
+    h2d = host_g.numel() * host_g.element_size()
+    K_e2e = max(3, min(100, int(5.0 / (h2d / 200e9 + 1e-4))))
     dev_g = [g, torch.empty_like(g)]
     up = torch.cuda.Stream(device)
     down = torch.cuda.Stream(device)
@@ -493,13 +651,7 @@ def run_e2e(z, wl, mode, g, master, m, v, params, stride, stream, device, dist, 
                 uploaded[nb].record(up)
         stream.wait_event(uploaded[b])
         stream.wait_event(downloaded)        # the previous parameters have left
-        t += 1
-        if wl.shard is None:
-            z.zero_adam_step(dev_g[b], stride, master, m, v, params, wl.N, wl.P, wl.stage, t,
-                             wl.lr, wl.b1, wl.b2, wl.eps, mode, stream)
-        else:
-            z.zero_adam_step_shard(dev_g[b], stride, 0, wl.shard, master, m, v, params, wl.N,
-                                   wl.P, wl.stage, t, wl.lr, wl.b1, wl.b2, wl.eps, mode, stream)
+        head.step(dev_g[b])
         consumed[b].record(stream)
         down.wait_event(consumed[b])
         with torch.cuda.stream(down):
@@ -509,11 +661,13 @@ def run_e2e(z, wl, mode, g, master, m, v, params, stride, stream, device, dist, 
     e1.record(stream)
     torch.cuda.synchronize()
     ms = dist.max(e0.elapsed_time(e1), device)
-    return {"value": wl.elems * K_e2e * dist.world / (ms / 1e3), "unit": "params/s",
-            "h2d_bytes_per_step": host_g.numel() * host_g.element_size(),
-            "d2h_bytes_per_step": host_p.numel() * host_p.element_size(),
-            "steps": K_e2e, "ms_per_step": ms / K_e2e,
-            "pipelining": "upload of step k+1 overlaps step k's kernel and download"}
+    out = {"value": head.wl.elems * K_e2e * dist.world / (ms / 1e3), "unit": "params/s",
+           "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": host_p.numel() * host_p.element_size(),
+           "steps": K_e2e, "ms_per_step": ms / K_e2e,
+           "pipelining": "upload of step k+1 overlaps step k's kernel and download"}
+    del dev_g, host_g, host_p
+    return out
 
 
 def run_overlap(args, wl, mode, dist):

@@ -411,7 +411,14 @@ int zero_mlp4_layer_grads(int32_t layer, const void* params_fp16, const float* x
  *  pipelined = 0 puts everything on main_stream in the same order.  Before
  *  returning, main_stream is made to wait for every update, so the next
  *  step's all-gather sees them.  All buffers are device memory.
- * Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
+ *  Every argument is checked before anything is enqueued: sizes and
+ *  hyper-parameters as for zero_adam_step_shard (ZERO_EINVAL), each buffer
+ *  aligned to its element size (ZERO_EALIGN), and no two of x [P][n],
+ *  gathered_fp16, master, m, v, shard_fp16, loss [P] and the gradients'
+ *  span ((P-1) rank_stride + 8 elements) sharing a byte (ZERO_EOVERLAP);
+ *  such a rejected call writes nothing.  A ZERO_ECUDA from the runtime part
+ *  way through may leave the work enqueued before it in place.
+ * Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_EOVERLAP, ZERO_ECUDA. */
 int zero_mlp4_zero3_step(const float* x, int32_t P, int32_t n, void* gathered_fp16, float* master,
                          float* m, float* v, void* shard_fp16, void* grads_fp16,
                          int64_t rank_stride, float* loss, int64_t t, float lr, float beta1,
@@ -431,19 +438,25 @@ int zero_mlp4_zero3_step(const float* x, int32_t P, int32_t n, void* gathered_fp
  * x, master / m / v, the owners' fp16 shards and loss, as for
  * zero_mlp4_zero3_step.
  *  - Limit: the array holds at most 8 ranks' gradients; P outside [1, 8]
- *    returns ZERO_EINVAL, as do the other bad arguments, before anything is
- *    enqueued.
+ *    returns ZERO_EINVAL.  Every argument is checked, as for
+ *    zero_mlp4_zero3_step (no two of x, master, m, v, shard_fp16 and loss
+ *    may share a byte, nor any of them a byte of the array), before
+ *    anything is enqueued: a rejected call writes nothing.
  *  - Schedule: the serial one (pipelined = 0) on cuda_stream; the call
  *    neither allocates nor creates events.
  *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and keeps it; make
- *    that first call before any stream capture.
+ *    (cudaGetSymbolAddress, with that device current) and keeps it together
+ *    with the identity of the device's context; a call that finds another
+ *    context current (after cudaDeviceReset, or once the primary context
+ *    was destroyed and created again, which can move the array) looks the
+ *    address up again.  Make the first call on a device, and the first after
+ *    a reset, before any stream capture.
  *  - Every call on a device uses the same array, which keeps the contents
  *    of the last call (each call writes every entry before reading it, so
  *    nothing needs clearing).  Calls whose work overlaps on the GPU -- on
  *    two streams, or from two host threads -- race on it: order them.
  * Errors: ZERO_EINVAL (also for a current device numbered 64 or above),
- * ZERO_EALIGN, ZERO_ECUDA. */
+ * ZERO_EALIGN, ZERO_EOVERLAP, ZERO_ECUDA. */
 int zero_mlp4_zero3_step_noalloc(const float* x, int32_t P, int32_t n, float* master, float* m,
                                  float* v, void* shard_fp16, float* loss, int64_t t, float lr,
                                  float beta1, float beta2, float eps, int32_t mode,

@@ -175,3 +175,57 @@ def test_mean_division_check_rejects_bad_ranges(zlib):
         with pytest.raises(zlib.ZeroError) as e:
             zlib.zero_selftest_mean_division(lo, hi)
         assert e.value.code == zlib.ZERO_EINVAL
+
+
+# the 4-layer MLP steps: made-up buffers, 4 KiB apart unless a case moves one
+X_, GATH, MST, MOM, VAR, SHD, GRD, LOSS = (A + (i << 12) for i in range(8))
+MLP_GOOD = dict(x=X_, P=4, n=16, gathered=GATH, master=MST, m=MOM, v=VAR, shard=SHD, grads=GRD,
+                rank_stride=8, loss=LOSS, t=1, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8, mode=0)
+
+
+def _mlp_regular(zlib, **kw):
+    a = dict(MLP_GOOD, **kw)
+    return zlib.lib().zero_mlp4_zero3_step(a["x"], a["P"], a["n"], a["gathered"], a["master"],
+                                           a["m"], a["v"], a["shard"], a["grads"],
+                                           a["rank_stride"], a["loss"], a["t"], a["lr"],
+                                           a["beta1"], a["beta2"], a["eps"], a["mode"], 0, 0, 0)
+
+
+def _mlp_noalloc(zlib, **kw):
+    a = dict(MLP_GOOD, **kw)
+    return zlib.lib().zero_mlp4_zero3_step_noalloc(a["x"], a["P"], a["n"], a["master"], a["m"],
+                                                   a["v"], a["shard"], a["loss"], a["t"],
+                                                   a["lr"], a["beta1"], a["beta2"], a["eps"],
+                                                   a["mode"], 0)
+
+
+MLP_BAD_BOTH = [
+    (dict(P=0), -1), (dict(P=9), -1), (dict(n=0), -1), (dict(t=0), -1), (dict(mode=5), -1),
+    (dict(lr=math.nan), -1), (dict(beta1=1.0), -1), (dict(eps=-1.0), -1),
+    (dict(x=None), -1), (dict(master=None), -1), (dict(m=None), -1), (dict(loss=None), -1),
+    (dict(master=MST + 2), -2), (dict(m=MOM + 1), -2), (dict(v=VAR + 2), -2),
+    (dict(loss=LOSS + 2), -2), (dict(x=X_ + 2), -2), (dict(shard=SHD + 1), -2),
+    # whole 8-element buffers that overlap, though no one shard's pieces would
+    (dict(m=MST + 8), -3), (dict(v=MOM + 28), -3), (dict(shard=VAR + 16), -3),
+    (dict(loss=MST + 28), -3), (dict(master=X_ + 4 * 63), -3),
+]
+
+
+@no_gpu
+@pytest.mark.parametrize("kw,code", MLP_BAD_BOTH + [
+    (dict(gathered=None), -1), (dict(grads=None), -1), (dict(rank_stride=7), -1),
+    (dict(gathered=GATH + 1), -2), (dict(grads=GRD + 1), -2),
+    (dict(gathered=SHD + 14), -3), (dict(grads=LOSS - 2 * 3 * 8 - 14), -3),
+    (dict(rank_stride=2048, loss=GRD + 2 * 2048 + 4), -3),
+])
+def test_mlp4_step_rejects_before_enqueueing(zlib, kw, code):
+    """Every argument check of the MLP step comes before its first CUDA call:
+    with made-up device addresses and no GPU, a rejected call returns its
+    status instead of a CUDA error from a copy or a launch."""
+    assert _mlp_regular(zlib, **kw) == code
+
+
+@no_gpu
+@pytest.mark.parametrize("kw,code", MLP_BAD_BOTH)
+def test_mlp4_noalloc_step_rejects_before_enqueueing(zlib, kw, code):
+    assert _mlp_noalloc(zlib, **kw) == code

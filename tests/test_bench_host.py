@@ -16,7 +16,9 @@ import bench  # noqa: E402
 
 def test_defaults():
     a = bench.parse_args([])
-    assert a.gpus == 1 and a.workload == "gpt2s" and a.warmup >= 3 and a.steps >= 100
+    # the headline is the largest workload that fits one GPU: 1.3e9 parameters at P = 16
+    assert a.gpus == 1 and a.workload == "tf1p3b" and a.warmup >= 3 and a.steps >= 100
+    assert not a.no_per_config
     with pytest.raises(SystemExit):
         bench.parse_args(["--warmup", "2"])
 
@@ -120,6 +122,39 @@ def test_reference_arm_prints_one_contract_line():
     assert d["value"] > 0 and d["higher_is_better"] is True and "workload" in d["config"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert cb["hardware_concurrency"] >= cb["affinity_cores"] >= cb["threads_used"] == cb["cores"]
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    # the same config object our arm prints for this workload; the sample is stated beside it
+    from zero_sharded_mixed_shard_gb300 import synth
+    wl = synth.WORKLOADS["tiny"]
+    assert d["config"] == bench.workload_config(wl, 0, bench.l2_flush_for(wl, 0))
+    assert "elements [0," in d["sample"]
+
+
+def test_cpu_baseline_leg_reports_threads_and_every_config():
+    """The oracle timing: all allowed cores and one thread on the headline
+    workload, and a labelled per-element rate for each other workload."""
+    from zero_sharded_mixed_shard_gb300 import synth
+    W = synth.WORKLOADS
+    cb = bench.cpu_baseline_leg(W["tiny"], 0, 1.0, [(W["gpt2s"], 0), (W["folded"], 2)])
+    hw, allowed = bench.host_cores()
+    assert cb["hardware_concurrency"] == hw and cb["affinity_cores"] == allowed
+    assert cb["threads_used"] == allowed == cb["cores"] and cb["value"] > 0
+    assert cb["single_thread"]["threads_used"] == 1 and cb["single_thread"]["value"] > 0
+    per = cb["per_config"]
+    assert per["gpt2s/mode0"]["kind"] == "whole step"
+    assert "extrapolated" in per["folded/mode2"]["kind"]
+    for e in per.values():
+        assert e["value"] > 0 and e["step_s"] > 0 and e["sample"]
+
+
+def test_oracle_inputs_repeat_a_draw_to_fill_a_sample():
+    import numpy as np
+    from zero_sharded_mixed_shard_gb300 import synth
+    wl = synth.WORKLOADS["gpt2s"]
+    codes, w, m, v = bench.oracle_inputs(wl, 10_000, draw=4096)
+    c = codes.reshape(wl.P, 10_000)
+    assert np.array_equal(c[:, 4096:8192], c[:, :4096]) and np.array_equal(w[4096:8192], w[:4096])
+    assert not m.any() and not v.any() and codes.size == wl.P * 10_000

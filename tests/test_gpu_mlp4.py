@@ -102,3 +102,32 @@ def test_layer_kernels_against_oracle(z):
         z.zero_mlp4_layer_grads(5, dp, dx, P, n, grads, 12)
     with pytest.raises(z.ZeroError):
         z.zero_mlp4_layer_grads(1, dp, dx, 9, n, grads, 12)
+
+
+def test_rejected_step_writes_nothing(z):
+    """Arguments are checked before anything is enqueued: a misaligned master
+    or whole buffers that overlap leave the loss, the gathered copy, the
+    gradients and the shards as they were."""
+    P, n = 4, 8
+    x = torch.rand((P, n), device="cuda")
+    master, m, v = torch.ones(8, device="cuda"), torch.zeros(8, device="cuda"), torch.zeros(8, device="cuda")
+    shard16 = torch.ones(8, dtype=torch.float16, device="cuda")
+    gathered16 = torch.full((8,), 7.0, dtype=torch.float16, device="cuda")
+    grads16 = torch.full((P, 8), 5.0, dtype=torch.float16, device="cuda")
+    loss = torch.full((P,), 123.0, device="cuda")
+    raw = torch.zeros(24, device="cuda")
+    keep = [t.clone() for t in (master, m, v, shard16, gathered16, grads16, loss)]
+    cases = [
+        (dict(master=raw.data_ptr() + 2), z.ZERO_EALIGN),
+        (dict(m=raw.data_ptr(), v=raw.data_ptr() + 16), z.ZERO_EOVERLAP),   # m [0, 32) and v [16, 48) bytes
+    ]
+    for kw, code in cases:
+        a = dict(master=master, m=m, v=v)
+        a.update(kw)
+        with pytest.raises(z.ZeroError) as e:
+            z.zero_mlp4_zero3_step(x, P, n, gathered16, a["master"], a["m"], a["v"], shard16, grads16, 8,
+                                   loss, 1, LR, B1, B2, EPS, 0, pipelined=True)
+        assert e.value.code == code, kw
+    torch.cuda.synchronize()
+    for t, u in zip((master, m, v, shard16, gathered16, grads16, loss), keep):
+        assert torch.equal(t, u)

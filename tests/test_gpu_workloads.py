@@ -1,13 +1,18 @@
 """The four full-size workloads, run through the same C-ABI calls the
-benchmark times, checked against the oracle on sampled windows.
+benchmark times, checked against the oracle.
 
-Elements never interact, so the oracle's result on a window of the flat
-vector equals the full problem's result there.  Windows: the first and last
-4,096 elements of every shard, +-256 elements around every tensor boundary
-of the structured vector, and 16 random windows of 65,536 elements.  The
-oracle carries its own window state from step to step; gradients are redrawn
-on the device every step.
+The GPT-2-small workload (124 M elements) is compared on whole arrays at
+every checked step.  The larger ones are compared on windows: elements never
+interact, so the oracle's result on a window of the flat vector equals the
+full problem's result there.  Windows: the first and last 4,096 elements of
+every shard, +-256 elements around every tensor boundary of the structured
+vector, the first tile (2,048 elements) of every CTA's last tile of the
+bulk-copy pipeline -- the far end of each CTA's walk -- and 64 random
+windows of 2^20 elements.  The oracle carries its own window state from step
+to step; gradients are redrawn on the device every step.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -17,6 +22,7 @@ from zero_sharded_mixed_shard_gb300 import synth
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
+THREADS = max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1))
 
 
 @pytest.fixture(scope="module")
@@ -27,7 +33,10 @@ def z(zlib, oracle_mod):
     torch.cuda.empty_cache()
 
 
-def windows(wl, seed=0):
+TILE = 2048          # elements per tile of the bulk-copy pipeline
+
+
+def windows(wl, seed=0, ctas=None, n_random=64, random_len=1 << 20):
     E = wl.elems
     r = []
     if wl.shard is None:
@@ -42,9 +51,16 @@ def windows(wl, seed=0):
         for n in wl.tensors[:-1]:
             pos += n
             r.append((max(0, pos - 256), min(E, pos + 256)))
+    if ctas:
+        # CTA c takes tiles c, c + ctas, ...: its last one is the largest such
+        # index below the tile count (buffers start 16-byte aligned: no head)
+        ntiles = -(-(E // 8 * 8) // TILE)
+        for c in range(min(ctas, ntiles)):
+            last = c + ((ntiles - 1 - c) // ctas) * ctas
+            r.append((last * TILE, min(E, (last + 1) * TILE)))
     rng = np.random.default_rng(seed)
-    for s in rng.integers(0, max(1, E - 65536), size=16):
-        r.append((int(s), int(min(E, s + 65536))))
+    for s in rng.integers(0, max(1, E - random_len), size=n_random):
+        r.append((int(s), int(min(E, s + random_len))))
     r.sort()
     merged = []
     for b, e in r:
@@ -55,11 +71,27 @@ def windows(wl, seed=0):
     return merged
 
 
+@pytest.mark.gpu
+def test_windows_cover_every_cta_last_tile():
+    """Host-side check of the window plan on the 1.3e9 vector at 152 CTAs."""
+    wl = synth.WORKLOADS["tf1p3b"]
+    w = windows(wl, 0, ctas=152)
+    ntiles = -(-wl.N // TILE)
+    for c in range(152):
+        last = c + ((ntiles - 1 - c) // 152) * 152
+        assert last + 152 >= ntiles
+        b = last * TILE
+        assert any(lo <= b and min(wl.N, b + TILE) <= hi for lo, hi in w), c
+    assert sum(e - b for b, e in w) >= 64 * (1 << 20) * 0.9
+
+
 def host_u16(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def run_workload(z, wl, mode, steps, check_steps, padded=True, kernel="bulk"):
+def run_workload(z, wl, mode, steps, check_steps, padded=True, kernel="bulk", whole=False):
+    """Run the workload's steps; check the windows (or, with ``whole``, every
+    element) against the oracle at the steps in ``check_steps``."""
     dev = "cuda"
     E, P = wl.elems, wl.P
     stride = wl.rank_stride(padded)
@@ -69,15 +101,18 @@ def run_workload(z, wl, mode, steps, check_steps, padded=True, kernel="bulk"):
     # (an unpadded rank stride puts the ranks off the 16-byte phase: vector kernel)
     plan = z.zero_step_plan(g, stride, master, m, v, params, E, P, wl.stage, mode)
     assert plan["kernel"] == kernel, (wl.name, plan)
-    wins = windows(wl, wl.seed)
+    wins = [(0, E)] if whole else windows(wl, wl.seed, ctas=plan["ctas"] if plan["kernel"] == "bulk" else None)
     ref = {w: [master[w[0]:w[1]].cpu().numpy(), m[w[0]:w[1]].cpu().numpy(),
                v[w[0]:w[1]].cpu().numpy()] for w in wins}
     worst = (0, 0)
     for t in range(1, steps + 1):
         synth.torch_grads(P, E, stride, wl.grad_sigma, wl.seed, dev, wl.heavy_tail_frac,
                           wl.zero_frac, step=t, out=g)
-        wg = {w: g[:, w[0]:w[1]].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-              for w in wins}
+        if whole:
+            wg = {(0, E): g[:, :E].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)}
+        else:
+            wg = {w: g[:, w[0]:w[1]].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+                  for w in wins}
         if wl.shard is None:
             z.zero_adam_step(g, stride, master, m, v, params, wl.N, P, wl.stage, t, wl.lr,
                              wl.b1, wl.b2, wl.eps, mode)
@@ -86,7 +121,7 @@ def run_workload(z, wl, mode, steps, check_steps, padded=True, kernel="bulk"):
                                    wl.stage, t, wl.lr, wl.b1, wl.b2, wl.eps, mode)
         for (b, e) in wins:
             p_ref = oracle.adam_elems(wg[(b, e)].reshape(-1), e - b, P, *ref[(b, e)], t, wl.lr,
-                                      wl.b1, wl.b2, wl.eps, mode, threads=4)
+                                      wl.b1, wl.b2, wl.eps, mode, threads=THREADS)
             if t in check_steps:
                 got = [master[b:e].cpu().numpy(), m[b:e].cpu().numpy(), v[b:e].cpu().numpy(),
                        host_u16(params[b:e])]
@@ -102,7 +137,7 @@ def run_workload(z, wl, mode, steps, check_steps, padded=True, kernel="bulk"):
 
 def test_gpt2s_workload(z):
     wl = synth.WORKLOADS["gpt2s"]
-    worst, _ = run_workload(z, wl, 0, wl.steps, check_steps={1, 2, 5, 10, wl.steps})
+    worst, _ = run_workload(z, wl, 0, wl.steps, check_steps={1, 2, 5, 10, wl.steps}, whole=True)
     assert worst == (0, 0)
     torch.cuda.empty_cache()
 

@@ -21,17 +21,22 @@
 // shards, and the next step's all-gather copies them into the gathered
 // vector.  One thread per rank: the model has 8 parameters and the point is
 // the schedule, not the arithmetic.
+#include <cuda.h> // driver types only: the two driver calls are found through the runtime
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "zero_step.h"
 
-// Shared with step.cu (not exported): keeps zero_last_cuda_error current.
+// Shared with step.cu (not exported): keeps zero_last_cuda_error current,
+// and the step's own validation of its sizes and hyper-parameters.
 __attribute__((visibility("hidden"))) int zero_record_cuda_error(int err);
+__attribute__((visibility("hidden"))) int zero_check_step_scalars(int64_t N, int32_t P, int32_t stage, int64_t t,
+                                                                  float lr, float b1, float b2, float eps,
+                                                                  int32_t mode);
 
 namespace {
 
@@ -129,6 +134,58 @@ __global__ void mlp4_layer_grads_kernel(int layer, const __half* p16, const floa
 
 int last_error(cudaError_t e) { return e == cudaSuccess ? ZERO_OK : zero_record_cuda_error(static_cast<int>(e)); }
 
+// One device buffer of a training step: its address and its size in bytes.
+struct Span {
+    uintptr_t at;
+    uintptr_t bytes;
+};
+
+// Every check of a training step's arguments, made before anything is
+// enqueued so that a rejected call leaves every buffer as it was: sizes,
+// hyper-parameters (as zero_adam_step_shard checks them), the alignment of
+// every buffer to its element size, and that no two buffers share a byte
+// (x is only read, but the kernels that read it run between writes of the
+// others).  gathered and grads are absent (NULL) for the no-allocation step,
+// whose scratch is inside the library.
+int check_mlp4_step(const float* x, int32_t P, int32_t n, const void* gathered, const float* master,
+                    const float* m, const float* v, const void* shard, const void* grads, int64_t rank_stride,
+                    const float* loss, int64_t t, float lr, float beta1, float beta2, float eps, int32_t mode,
+                    bool caller_scratch)
+{
+    if (P < 1 || P > kMaxRanks || n < 1) return ZERO_EINVAL;
+    int rc = zero_check_step_scalars(kParams, P, 3, t, lr, beta1, beta2, eps, mode);
+    if (rc) return rc;
+    if (!x || !master || !m || !v || !shard || !loss) return ZERO_EINVAL;
+    if (caller_scratch && (!gathered || !grads || rank_stride < kParams || rank_stride > (INT64_MAX >> 4)))
+        return ZERO_EINVAL;
+    const uintptr_t f4[] = {reinterpret_cast<uintptr_t>(x), reinterpret_cast<uintptr_t>(master),
+                            reinterpret_cast<uintptr_t>(m), reinterpret_cast<uintptr_t>(v),
+                            reinterpret_cast<uintptr_t>(loss)};
+    for (uintptr_t a : f4)
+        if (a % 4) return ZERO_EALIGN;
+    if (reinterpret_cast<uintptr_t>(shard) % 2) return ZERO_EALIGN;
+    if (caller_scratch && (reinterpret_cast<uintptr_t>(gathered) % 2 || reinterpret_cast<uintptr_t>(grads) % 2))
+        return ZERO_EALIGN;
+    Span spans[8];
+    int ns = 0;
+    spans[ns++] = Span{reinterpret_cast<uintptr_t>(x), static_cast<uintptr_t>(P) * static_cast<uintptr_t>(n) * 4};
+    spans[ns++] = Span{reinterpret_cast<uintptr_t>(master), kParams * 4};
+    spans[ns++] = Span{reinterpret_cast<uintptr_t>(m), kParams * 4};
+    spans[ns++] = Span{reinterpret_cast<uintptr_t>(v), kParams * 4};
+    spans[ns++] = Span{reinterpret_cast<uintptr_t>(shard), kParams * 2};
+    spans[ns++] = Span{reinterpret_cast<uintptr_t>(loss), static_cast<uintptr_t>(P) * 4};
+    if (caller_scratch) {
+        spans[ns++] = Span{reinterpret_cast<uintptr_t>(gathered), kParams * 2};
+        spans[ns++] = Span{reinterpret_cast<uintptr_t>(grads),
+                           (static_cast<uintptr_t>(P - 1) * static_cast<uintptr_t>(rank_stride) + kParams) * 2};
+    }
+    for (int i = 0; i < ns; ++i)
+        for (int j = i + 1; j < ns; ++j)
+            if (spans[i].at < spans[j].at + spans[j].bytes && spans[j].at < spans[i].at + spans[i].bytes)
+                return ZERO_EOVERLAP;
+    return ZERO_OK;
+}
+
 } // namespace
 
 extern "C" int zero_mlp4_loss(const void* params_fp16, const float* x, int32_t P, int32_t n, float* loss,
@@ -156,8 +213,9 @@ extern "C" int zero_mlp4_zero3_step(const float* x, int32_t P, int32_t n, void* 
                                     float* loss, int64_t t, float lr, float beta1, float beta2, float eps,
                                     int32_t mode, int32_t pipelined, void* main_stream, void* step_stream)
 {
-    if (!x || !gathered_fp16 || !master || !m || !v || !shard_fp16 || !grads_fp16 || !loss) return ZERO_EINVAL;
-    if (P < 1 || P > kMaxRanks || n < 1 || rank_stride < kParams || t < 1) return ZERO_EINVAL;
+    int rc = check_mlp4_step(x, P, n, gathered_fp16, master, m, v, shard_fp16, grads_fp16, rank_stride, loss, t,
+                             lr, beta1, beta2, eps, mode, true);
+    if (rc) return rc;
     cudaStream_t ms = static_cast<cudaStream_t>(main_stream);
     cudaStream_t ss = pipelined ? static_cast<cudaStream_t>(step_stream) : ms;
     const int64_t M = (kParams + P - 1) / P;
@@ -189,7 +247,7 @@ extern "C" int zero_mlp4_zero3_step(const float* x, int32_t P, int32_t n, void* 
     if ((e = cudaMemcpyAsync(gathered, shards, kParams * sizeof(__half), cudaMemcpyDeviceToDevice, ms)) !=
         cudaSuccess)
         return fail(e);
-    int rc = zero_mlp4_loss(gathered, x, P, n, loss, ms);
+    rc = zero_mlp4_loss(gathered, x, P, n, loss, ms);
     if (rc) {
         cleanup();
         return rc;
@@ -244,21 +302,75 @@ static_assert(kScratchGrads + kMaxRanks * kScratchRankStride <= kScratchHalves, 
 
 static __device__ __align__(256) __half g_mlp4_scratch[kScratchHalves];
 
-// Device address of g_mlp4_scratch, looked up once per device with that
-// device current.  Host code may not use the symbol's name as an address.
-std::atomic<void*> g_scratch_addr[64];
+// Identity of the context current on this host thread, 0 when none is
+// current or the driver cannot say.  The driver's cuCtxGetCurrent and
+// cuCtxGetId are reached through the runtime's entry-point lookup, so the
+// library needs no link against the driver library.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+unsigned long long current_context_id()
+{
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult found = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &found) ==
+                cudaSuccess &&
+            found == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        found = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &found) == cudaSuccess &&
+            found == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+// Device address of g_mlp4_scratch per device, looked up with that device
+// current and kept together with the identity of the context it belongs to.
+// Host code may not use the symbol's name as an address.  A device reset
+// (cudaDeviceReset, or the primary context torn down and created again) can
+// load the library's module at another address; the new context has a new
+// identity, so the address is looked up again instead of used stale.
+struct ScratchSlot {
+    unsigned long long ctx;
+    void* addr;
+};
+constexpr int kScratchDevices = 64;
+std::mutex g_scratch_mu;
+ScratchSlot g_scratch_slot[kScratchDevices];
 
 int scratch_address(void** out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return zero_record_cuda_error(static_cast<int>(e));
-    if (dev < 0 || dev >= 64) return ZERO_EINVAL;
-    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
-        e = cudaGetSymbolAddress(&p, g_mlp4_scratch);
-        if (e != cudaSuccess) return zero_record_cuda_error(static_cast<int>(e));
-        g_scratch_addr[dev].store(p, std::memory_order_release);
+    if (dev < 0 || dev >= kScratchDevices) return ZERO_EINVAL;
+    const unsigned long long ctx = current_context_id();
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        const ScratchSlot& s = g_scratch_slot[dev];
+        if (ctx != 0 && s.ctx == ctx && s.addr) {
+            *out = s.addr;
+            return ZERO_OK;
+        }
+    }
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_mlp4_scratch);
+    if (e != cudaSuccess) return zero_record_cuda_error(static_cast<int>(e));
+    // the lookup makes the device's primary context current if it was not
+    const unsigned long long now = ctx != 0 ? ctx : current_context_id();
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        g_scratch_slot[dev] = ScratchSlot{now, p};
     }
     *out = p;
     return ZERO_OK;
@@ -270,15 +382,25 @@ extern "C" int zero_mlp4_zero3_step_noalloc(const float* x, int32_t P, int32_t n
                                             float* v, void* shard_fp16, float* loss, int64_t t, float lr,
                                             float beta1, float beta2, float eps, int32_t mode, void* cuda_stream)
 {
-    // the scratch holds at most kMaxRanks ranks' gradients
-    if (P < 1 || P > kMaxRanks) return ZERO_EINVAL;
-    if (!x || !master || !m || !v || !shard_fp16 || !loss || n < 1 || t < 1) return ZERO_EINVAL;
-    if (mode < 0 || mode > ZERO_MODE_MOMENTUM || !isfinite(lr) || !isfinite(beta1) || !isfinite(beta2) ||
-        !isfinite(eps) || !(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f) || !(eps >= 0.0f))
-        return ZERO_EINVAL; // refused before anything is enqueued
-    void* scratch = nullptr;
-    int rc = scratch_address(&scratch);
+    // every argument is checked before anything is enqueued (P above
+    // kMaxRanks: more ranks' gradients than the scratch holds)
+    int rc = check_mlp4_step(x, P, n, nullptr, master, m, v, shard_fp16, nullptr, 0, loss, t, lr, beta1, beta2, eps,
+                             mode, false);
     if (rc) return rc;
+    void* scratch = nullptr;
+    rc = scratch_address(&scratch);
+    if (rc) return rc;
+    // no caller buffer may lie inside the scratch
+    const uintptr_t sb = reinterpret_cast<uintptr_t>(scratch), se = sb + sizeof(g_mlp4_scratch);
+    const uintptr_t ends[][2] = {
+        {reinterpret_cast<uintptr_t>(x), static_cast<uintptr_t>(P) * static_cast<uintptr_t>(n) * 4},
+        {reinterpret_cast<uintptr_t>(master), kParams * 4},
+        {reinterpret_cast<uintptr_t>(m), kParams * 4},
+        {reinterpret_cast<uintptr_t>(v), kParams * 4},
+        {reinterpret_cast<uintptr_t>(shard_fp16), kParams * 2},
+        {reinterpret_cast<uintptr_t>(loss), static_cast<uintptr_t>(P) * 4}};
+    for (const auto& b : ends)
+        if (b[0] < se && sb < b[0] + b[1]) return ZERO_EOVERLAP;
     __half* gathered = static_cast<__half*>(scratch);
     __half* grads = gathered + kScratchGrads;
     // the serial schedule of zero_mlp4_zero3_step on one stream: it creates
