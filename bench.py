@@ -389,8 +389,10 @@ def run_reference(args, wl, mode, dist):
 def l2_flush_for(wl, mode) -> int | None:
     """Bytes written between timed steps to flush L2, or None: a step that
     moves less than twice the L2 would partly run from L2 when repeated, so
-    a buffer of 4x the L2 is written between its timed steps and only the
-    steps themselves are timed."""
+    a buffer of 4x the L2 is written between its timed steps, then another
+    one of 4x the L2 is read (so the L2 holds clean lines of neither the
+    step's buffers nor the flush's: the step pays for no write-back of the
+    flush's dirty lines), and only the steps themselves are timed."""
     from zero_sharded_mixed_shard_gb300 import synth
     alg = wl.elems * synth.bytes_per_elem(wl.P, mode)
     return 4 * L2_BYTES if alg < 2 * L2_BYTES else None
@@ -400,8 +402,9 @@ def workload_config(wl, mode, l2_flush_bytes=None):
     from zero_sharded_mixed_shard_gb300 import synth
     step_gb = wl.elems * synth.bytes_per_elem(wl.P, mode) / 1e9
     if l2_flush_bytes:
-        l2 = (f"L2 flushed between timed steps ({l2_flush_bytes / 1e6:.0f} MB written; a step "
-              f"moves only {step_gb * 1e3:.1f} MB); value from the summed per-step event times")
+        l2 = (f"L2 flushed between timed steps ({l2_flush_bytes / 1e6:.0f} MB written, then "
+              f"{l2_flush_bytes / 1e6:.0f} MB read; a step moves only {step_gb * 1e3:.1f} MB); "
+              f"value from the summed per-step event times")
     else:
         l2 = f"inputs larger than L2: {step_gb:.2f} GB moved per step"
     cfg = {"workload": f"{wl.name}: N={wl.N:,} P={wl.P} ZeRO-{wl.stage} "
@@ -441,7 +444,13 @@ class Timed:
         self.alg_bytes = E * synth.bytes_per_elem(P, mode)
         fb = l2_flush_for(wl, mode)
         self.flush = torch.empty(fb, dtype=torch.uint8, device=device) if fb else None
+        self.flush_read = torch.ones(fb // 4, dtype=torch.float32, device=device) if fb else None
         self.t = 0
+
+    def flush_l2(self):
+        if self.flush is not None:
+            self.flush.zero_()
+            self.flush_read.sum()
 
     def step(self, g=None):
         wl, z = self.wl, self.z
@@ -458,8 +467,7 @@ class Timed:
     def warm(self, W):
         import torch
         for _ in range(W):
-            if self.flush is not None:
-                self.flush.zero_()
+            self.flush_l2()
             self.step()
         torch.cuda.synchronize()
 
@@ -471,8 +479,7 @@ class Timed:
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
         for i in range(K):
-            if self.flush is not None:
-                self.flush.zero_()
+            self.flush_l2()
             starts[i].record(self.stream)
             self.step()
             ends[i].record(self.stream)
@@ -483,8 +490,26 @@ class Timed:
 
     def free(self):
         import torch
-        self.g = self.master = self.m = self.v = self.params = self.flush = None
+        self.g = self.master = self.m = self.v = self.params = self.flush = self.flush_read = None
         torch.cuda.empty_cache()
+
+
+def one_element_step_ms(z, wl, mode, K, dist, device, stream) -> float:
+    """Mean event-to-event time of a step of ONE element with the workload's
+    P and mode, under the same L2 flush: the fixed cost of a launch through
+    the library (enqueue to completion), against which a small workload's
+    own time can be read."""
+    import torch
+    one = dataclasses.replace(wl, N=1, shard=None, tensors=None, name=wl.name + "-N1")
+    leg = Timed(z, one, mode, dist, device, stream)
+    if leg.flush is None:          # flush as the small workload does
+        fb = 4 * L2_BYTES
+        leg.flush = torch.empty(fb, dtype=torch.uint8, device=device)
+        leg.flush_read = torch.ones(fb // 4, dtype=torch.float32, device=device)
+    leg.warm(3)
+    _, ms = leg.run(K)
+    leg.free()
+    return ms
 
 
 def roofline_entry(wl, mode, plan, alg_bytes, mean_launch_ms):
@@ -555,12 +580,19 @@ def run_ours(args, wl, mode, dist):
             r_ms, l_ms = leg.run(ck)
             dist.barrier()
             r_ms, l_ms = dist.max(r_ms, device), dist.max(l_ms, device)
+            extra = {}
+            if leg.flush is not None:   # a small workload: how much of its time is the launch
+                floor = dist.max(one_element_step_ms(z, cwl, cmode, ck, dist, device, stream), device)
+                extra = {"one_element_step_ms": floor,
+                         "gbs_above_one_element_step": leg.alg_bytes / ((l_ms - floor) / 1e3) / 1e9
+                         if l_ms > floor else None}
             per_config[f"{name}/mode{cmode}"] = {
                 "workload": workload_config(cwl, cmode, None if leg.flush is None else leg.flush.numel())["workload"],
                 "value": cwl.elems * ck * dist.world / (r_ms / 1e3), "unit": "params/s", "steps": ck,
                 "ms_per_step": r_ms / ck,
                 "roofline": roofline_entry(cwl, cmode, leg.plan, leg.alg_bytes, l_ms),
-                "l2": "flushed between timed steps" if leg.flush is not None else "inputs larger than L2"}
+                "l2": "flushed between timed steps" if leg.flush is not None else "inputs larger than L2",
+                **extra}
             leg.free()
             del leg
         p1 = time.time()

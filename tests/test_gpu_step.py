@@ -337,7 +337,7 @@ def _assert_path(z, kernel, g, stride, s, N, P, mode=0):
     assert plan["kernel"] == kernel, plan
 
 
-@pytest.mark.parametrize("P", [1, 2, 3, 4, 6, 8, 13, 16, 33, 64, 72, 128, 144, 256])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 6, 7, 8, 9, 13, 16, 17, 24, 33, 64, 72, 100, 128, 144, 256])
 def test_tma_path_matches_oracle(z, P):
     """P that fills whole 8-rank chunks and P that leaves a partial last chunk;
     every kind of instance (P = 1, 2, 4, 8, 16, 64, 72, 128, 144, 256 of their

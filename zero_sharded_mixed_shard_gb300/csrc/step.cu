@@ -380,10 +380,13 @@ __global__ void __launch_bounds__(kThreads, vector_min_blocks(PT)) zero_fused_st
 // (tile, chunk of kChunkRanks ranks): one bulk copy of kTile*2 bytes per rank
 // of the chunk, plus the tile's master / m / v rows with the first chunk, all
 // landing in one of kStages shared-memory stages and counted by that stage's
-// mbarrier.  One elected thread issues the copies; every thread then reads its
-// 8 elements of each row from shared memory, accumulates the chunk's ranks in
-// rank order, and after the last chunk runs Adam and stores the results with
-// 16-byte streaming stores.  Copies of whole 4 KB rows keep the copy engine's
+// mbarrier.  Warp 0 issues the copies (thread 0 alone when a tile is one
+// chunk, one row per lane otherwise); every thread then reads its elements of
+// each row from shared memory, accumulates the chunk's ranks in rank order,
+// and after the last chunk runs Adam and stores the results with streaming
+// stores.  With P known only at run time, the last chunk's rank count is a
+// compile-time parameter and each tile's first and last chunks are peeled,
+// so every chunk is summed by straight-line code.  Copies of whole 4 KB rows keep the copy engine's
 // issue rate far from the limit and keep every DRAM stream long and sequential.
 // ---------------------------------------------------------------------------
 
@@ -493,10 +496,46 @@ __device__ __forceinline__ void accumulate_rows(float (&acc)[E], const unsigned 
     for (int q = 0; q < R; ++q) accumulate<E>(acc, smem_halves<E>(row + static_cast<size_t>(q) * kTile * 2));
 }
 
+// After a tile's last chunk of ranks: the gradient means, Adam and the
+// stores of this thread's E elements starting at element i of the range.
+template <int MODE, int PT, int E, int G>
+__device__ __forceinline__ void finish_tile(const StepArgs& a, const float (&acc)[E], float (&w)[E], float (&m)[E],
+                                            float (&v)[E], long long i, float* w0, float* m0, float* v0, __half* p0)
+{
+    float gm[E];
+    bool special = false;
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        gm[j] = finish_mean<PT>(acc[j], a);
+        if constexpr (MODE <= ZERO_MODE_FOLDED_STORAGE) // the only modes that divide
+            special |= !(isfinite(gm[j]) && isfinite(m[j]) && isfinite(v[j])) || gm[j] == 0.0f;
+    }
+    // G = 2: the shortcuts for infinite and zero operands are taken only
+    // by warps in which some lane holds a non-finite gradient mean or
+    // moment, or a zero gradient mean (what makes the numerators zero);
+    // one warp-uniform branch, and both branches give the same IEEE
+    // results
+    if (G == 1 || (G == 2 && __any_sync(__activemask(), special))) {
+#pragma unroll
+        for (int j = 0; j < E; ++j) adam_elem<MODE, 1>(a, gm[j], w[j], m[j], v[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < E; ++j) adam_elem<MODE, 0>(a, gm[j], w[j], m[j], v[j]);
+    }
+    store_floats<E>(w0 + i, w);
+    if constexpr (uses_m(MODE)) store_floats<E>(m0 + i, m);
+    if constexpr (uses_v(MODE)) store_floats<E>(v0 + i, v);
+    store_halves<E>(p0 + i, w); // all-gather: element head + i of the full vector
+}
+
 // NT consumer threads, E = kTile / NT consecutive elements each per tile.
-template <int MODE, int PT, int NT, int G>
+// PT > 0: P known at compile time.  PT = 0: P read at run time, with RL
+// (1..8) the rank count of the last chunk known at compile time, so P =
+// 8 (nch - 1) + RL for the run-time chunk count nch.
+template <int MODE, int PT, int NT, int G, int RL = 0>
 __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepArgs a)
 {
+    static_assert((PT > 0) == (RL == 0) && RL >= 0 && RL <= kChunkRanks, "RL only with a run-time P");
     constexpr int E = kTile / NT;
     static_assert(E * NT == kTile && (E == 2 || E == 4 || E == 8), "tile split over the threads");
     extern __shared__ __align__(128) unsigned char smem[];
@@ -524,8 +563,8 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
     }
+    if (tid < 32) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
     __syncthreads();
 
     const __half* g0 = a.g + a.head;
@@ -541,9 +580,16 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
     // same tile, else chunk 0 of this CTA's next tile).  Measured: counters
     // in the compile-time instances cost P = 16 and 64 20-25 %.
     auto tile_of = [&](long long u) { return blockIdx.x + (u / nch) * gridDim.x; };
-    int issue_c = 0;                   // generic instance, thread 0: chunk of the next unit to issue
+    int issue_c = 0;                   // generic instance, warp 0: chunk of the next unit to issue
     long long issue_tile = blockIdx.x; // and its tile
-    auto issue = [&](long long u) {    // thread 0 only, for u = 0, 1, 2, ... in turn
+    // Who issues a unit's copies.  With more than one chunk per tile, the 32
+    // lanes of warp 0, one row each (measured: P = 12 0.887 -> 0.929, 24
+    // 0.945 -> 1.025, 33 0.860 -> 0.972, 96 0.931 -> 1.007 of the copy
+    // roofline; 16 and 32 unchanged).  With one chunk, thread 0 alone, in
+    // the order below (lanes cost P = 8 0.984 -> 0.907 and P = 5 1 %):
+    // warp 0 is also a consumer, and the serial issue delays it least there.
+    const bool lane_issue = PT > 0 ? PT > kChunkRanks : nch > 1;
+    auto issue = [&](long long u) {    // the lanes of warp 0, for u = 0, 1, 2, ... in turn
         const int s = static_cast<int>(u % kStages);
         int c;
         long long i0;
@@ -563,6 +609,25 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
         const uint32_t hb = static_cast<uint32_t>(len) * 2, fb = static_cast<uint32_t>(len) * 4;
         unsigned char* st = smem + static_cast<size_t>(s) * kStageBytes;
         const uint32_t poison = (u == 0 && blockIdx.x == 0) ? a.poison_tx : 0u;
+        if (lane_issue) {
+            // one row per lane: gradient rows on lanes 0..rc-1, the state rows
+            // of a tile's first chunk on lanes 8, 9, 10, all issued at once
+            if (tid == 0) mbar_arrive_expect_tx(&full[s], hb * rc + (c == 0 ? state_rows(MODE) * fb : 0) + poison);
+            __syncwarp();
+            if (tid < rc) {
+                const __half* src = g0 + (static_cast<long long>(c) * kChunkRanks + tid) * a.stride + i0;
+                bulk_load(st + static_cast<size_t>(tid) * kTile * 2, src, hb, &full[s], policy);
+            } else if (c == 0) {
+                if (tid == kChunkRanks) bulk_load(st + kGradBytes, w0 + i0, fb, &full[s], policy);
+                if constexpr (uses_m(MODE))
+                    if (tid == kChunkRanks + 1) bulk_load(st + kGradBytes + kTile * 4, m0 + i0, fb, &full[s], policy);
+                if constexpr (uses_v(MODE))
+                    if (tid == kChunkRanks + 2)
+                        bulk_load(st + kGradBytes + 2 * kTile * 4, v0 + i0, fb, &full[s], policy);
+            }
+            return;
+        }
+        if (tid != 0) return;
         mbar_arrive_expect_tx(&full[s], hb * rc + (c == 0 ? state_rows(MODE) * fb : 0) + poison);
         const __half* src = g0 + static_cast<long long>(c) * kChunkRanks * a.stride + i0;
         // the larger group of rows first (measured: with few ranks the state
@@ -581,91 +646,96 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
         if (c == 0 && !state_first) load_state();
     };
 
-    if (tid == 0)
+    if (tid < 32)
         for (long long u = 0; u < kStages && u < units; ++u) issue(u);
 
     float acc[E], w[E], m[E] = {}, v[E] = {};
     long long u = 0;
-    int c_run = 0;                   // generic instance: chunk of ranks of unit u
-    long long tile_run = blockIdx.x; // and its tile
     bool failed = false;
-    for (; u < units; ++u) {
-        const int s = static_cast<int>(u % kStages);
-        const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>((u / kStages) & 1));
-        // one decision for the whole CTA; also: every thread is done with unit u-1
-        if (__syncthreads_or(!ok)) {
-            failed = true;
-            break;
-        }
-        if (tid == 0 && u >= 1 && u - 1 + kStages < units) issue(u - 1 + kStages);
-
-        const int c = PT > 0 ? static_cast<int>(u % nch) : c_run;
-        const long long i0 = (PT > 0 ? tile_of(u) : tile_run) * kTile;
-        const long long len = nbulk - i0 < kTile ? nbulk - i0 : kTile;
-        const unsigned char* st = smem + static_cast<size_t>(s) * kStageBytes;
-        const int e0 = tid * E;
-        if (e0 < len) {
-            if (c == 0) {
+    const int e0 = tid * E;
+    // Wait for unit uu's stage (every thread), then refill the stage of
+    // unit uu-1, which every thread has finished once the barrier passes.
+    // False if the wait gave up (one decision for the whole CTA).
+    auto wait_unit = [&](long long uu) -> bool {
+        const int s = static_cast<int>(uu % kStages);
+        const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>((uu / kStages) & 1));
+        if (__syncthreads_or(!ok)) return false;
+        if (tid < 32 && uu >= 1 && uu - 1 + kStages < units) issue(uu - 1 + kStages);
+        return true;
+    };
+    auto stage_of = [&](long long uu) { return smem + static_cast<size_t>(uu % kStages) * kStageBytes; };
+    auto load_state = [&](const unsigned char* st) {
 #pragma unroll
-                for (int j = 0; j < E; ++j) acc[j] = 0.0f;
-                smem_floats<E>(st + kGradBytes + e0 * 4, w);
-                if constexpr (uses_m(MODE)) smem_floats<E>(st + kGradBytes + kTile * 4 + e0 * 4, m);
-                if constexpr (uses_v(MODE)) smem_floats<E>(st + kGradBytes + 2 * kTile * 4 + e0 * 4, v);
+        for (int j = 0; j < E; ++j) acc[j] = 0.0f;
+        smem_floats<E>(st + kGradBytes + e0 * 4, w);
+        if constexpr (uses_m(MODE)) smem_floats<E>(st + kGradBytes + kTile * 4 + e0 * 4, m);
+        if constexpr (uses_v(MODE)) smem_floats<E>(st + kGradBytes + 2 * kTile * 4 + e0 * 4, v);
+    };
+
+    if constexpr (PT > 0) {
+        for (; u < units; ++u) {
+            if (!wait_unit(u)) {
+                failed = true;
+                break;
             }
-            // ranks c*8 .. c*8+rc-1 of this tile, in rank order
-            const int rc = P - c * kChunkRanks < kChunkRanks ? P - c * kChunkRanks : kChunkRanks;
-            if constexpr (PT > 0) {
+            const int c = static_cast<int>(u % nch);
+            const long long i0 = tile_of(u) * kTile;
+            const long long len = nbulk - i0 < kTile ? nbulk - i0 : kTile;
+            const unsigned char* st = stage_of(u);
+            if (e0 < len) {
+                if (c == 0) load_state(st);
+                // ranks c*8 .. c*8+rc-1 of this tile, in rank order
+                const int rc = P - c * kChunkRanks < kChunkRanks ? P - c * kChunkRanks : kChunkRanks;
 #pragma unroll
                 for (int q = 0; q < kChunkRanks; ++q)
                     if (q < rc) accumulate<E>(acc, smem_halves<E>(st + static_cast<size_t>(q) * kTile * 2 + e0 * 2));
-            } else {
-                // rc known only at run time (uniform over the CTA): one fully
-                // unrolled body per possible count
-                const unsigned char* row = st + static_cast<size_t>(e0) * 2;
-                switch (rc) {
-                case 8: accumulate_rows<E, 8>(acc, row); break;
-                case 7: accumulate_rows<E, 7>(acc, row); break;
-                case 6: accumulate_rows<E, 6>(acc, row); break;
-                case 5: accumulate_rows<E, 5>(acc, row); break;
-                case 4: accumulate_rows<E, 4>(acc, row); break;
-                case 3: accumulate_rows<E, 3>(acc, row); break;
-                case 2: accumulate_rows<E, 2>(acc, row); break;
-                default: accumulate_rows<E, 1>(acc, row); break;
-                }
-            }
-            if (c == nch - 1) {
-                float gm[E];
-                bool special = false;
-#pragma unroll
-                for (int j = 0; j < E; ++j) {
-                    gm[j] = finish_mean<PT>(acc[j], a);
-                    if constexpr (MODE <= ZERO_MODE_FOLDED_STORAGE) // the only modes that divide
-                        special |= !(isfinite(gm[j]) && isfinite(m[j]) && isfinite(v[j])) || gm[j] == 0.0f;
-                }
-                // G = 2: the shortcuts for infinite and zero operands are taken only
-                // by warps in which some lane holds a non-finite gradient mean or
-                // moment, or a zero gradient mean (what makes the numerators zero);
-                // one warp-uniform branch, and both branches give the same IEEE
-                // results
-                if (G == 1 || (G == 2 && __any_sync(__activemask(), special))) {
-#pragma unroll
-                    for (int j = 0; j < E; ++j) adam_elem<MODE, 1>(a, gm[j], w[j], m[j], v[j]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < E; ++j) adam_elem<MODE, 0>(a, gm[j], w[j], m[j], v[j]);
-                }
-                const long long i = i0 + e0;
-                store_floats<E>(w0 + i, w);
-                if constexpr (uses_m(MODE)) store_floats<E>(m0 + i, m);
-                if constexpr (uses_v(MODE)) store_floats<E>(v0 + i, v);
-                store_halves<E>(p0 + i, w); // all-gather: element head + i of the full vector
+                if (c == nch - 1) finish_tile<MODE, PT, E, G>(a, acc, w, m, v, i0 + e0, w0, m0, v0, p0);
             }
         }
-        if constexpr (PT == 0) {
-            if (++c_run == nch) {
-                c_run = 0;
-                tile_run += gridDim.x;
+    } else {
+        // Run-time P: each tile's units walked as its first chunk (with the
+        // state rows), the full middle chunks and the last chunk of RL
+        // ranks, so every chunk's rank count is known where it is summed.
+        for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            const long long i0 = tile * kTile;
+            const long long len = nbulk - i0 < kTile ? nbulk - i0 : kTile;
+            const bool mine = e0 < len;
+            if (!wait_unit(u)) {
+                failed = true;
+                break;
             }
+            const unsigned char* st = stage_of(u);
+            if (nch == 1) { // P = RL: one unit per tile
+                if (mine) {
+                    load_state(st);
+                    accumulate_rows<E, RL>(acc, st + static_cast<size_t>(e0) * 2);
+                    finish_tile<MODE, PT, E, G>(a, acc, w, m, v, i0 + e0, w0, m0, v0, p0);
+                }
+                ++u;
+                continue;
+            }
+            if (mine) {
+                load_state(st);
+                accumulate_rows<E, kChunkRanks>(acc, st + static_cast<size_t>(e0) * 2);
+            }
+            ++u;
+            for (int c = 1; c < nch - 1; ++c, ++u) {
+                if (!wait_unit(u)) {
+                    failed = true;
+                    break;
+                }
+                if (mine) accumulate_rows<E, kChunkRanks>(acc, stage_of(u) + static_cast<size_t>(e0) * 2);
+            }
+            if (failed) break;
+            if (!wait_unit(u)) {
+                failed = true;
+                break;
+            }
+            if (mine) {
+                accumulate_rows<E, RL>(acc, stage_of(u) + static_cast<size_t>(e0) * 2);
+                finish_tile<MODE, PT, E, G>(a, acc, w, m, v, i0 + e0, w0, m0, v0, p0);
+            }
+            ++u;
         }
     }
 
@@ -737,10 +807,11 @@ KernelFn pick_kernel(int mode, int V, int P)
 // Consumer width of the bulk-copy kernel by P (measured on GB300): with few
 // ranks per tile the Adam arithmetic dominates and wants more warps; with
 // 8 ranks one 16-byte shared-memory read per rank per thread is best; with
-// more ranks the rank reduction wants more warps again.
+// 5-7 (256 consumers cost them 20 %) and with more ranks the rank reduction
+// wants more warps again.
 constexpr int tma_threads(int P)
 {
-    return P <= 4 ? 1024 : (P <= 8 ? 256 : 512);
+    return P <= 4 ? 1024 : (P == 8 ? 256 : 512);
 }
 
 struct TmaKernel {
@@ -755,21 +826,41 @@ TmaKernel tma_instance()
     return TmaKernel{zero_fused_step_tma_kernel<MODE, PT, NT, 2>, NT};
 }
 
-// Rank counts without an instance of their own, with P read at run time:
-// 1024 consumers up to 4 ranks, 512 above.
-template <int MODE, int NT>
-TmaKernel tma_generic()
+// Rank counts above 8 without an instance of their own: P read at run time,
+// the last chunk's rank count RL = P - 8 (nch - 1) at compile time, 512
+// consumers.
+template <int MODE, int RL>
+TmaKernel tma_generic_rl()
 {
-    return TmaKernel{zero_fused_step_tma_kernel<MODE, 0, NT, 2>, NT};
+    return TmaKernel{zero_fused_step_tma_kernel<MODE, 0, tma_threads(64), 2, RL>, tma_threads(64)};
+}
+
+template <int MODE>
+TmaKernel tma_generic(int P)
+{
+    switch (P - ((P - 1) / kChunkRanks) * kChunkRanks) {
+    case 1: return tma_generic_rl<MODE, 1>();
+    case 2: return tma_generic_rl<MODE, 2>();
+    case 3: return tma_generic_rl<MODE, 3>();
+    case 4: return tma_generic_rl<MODE, 4>();
+    case 5: return tma_generic_rl<MODE, 5>();
+    case 6: return tma_generic_rl<MODE, 6>();
+    case 7: return tma_generic_rl<MODE, 7>();
+    default: return tma_generic_rl<MODE, 8>();
+    }
 }
 
 template <int MODE>
 TmaKernel pick_tma_p(int P)
 {
     switch (P) {
-    case 1: return tma_instance<MODE, 1>();
+    case 1: return tma_instance<MODE, 1>(); // every P up to one chunk of 8 ranks
     case 2: return tma_instance<MODE, 2>();
+    case 3: return tma_instance<MODE, 3>();
     case 4: return tma_instance<MODE, 4>();
+    case 5: return tma_instance<MODE, 5>();
+    case 6: return tma_instance<MODE, 6>();
+    case 7: return tma_instance<MODE, 7>();
     case 8: return tma_instance<MODE, 8>();
     case 16: return tma_instance<MODE, 16>();
     case 32: return tma_instance<MODE, 32>();
@@ -778,9 +869,8 @@ TmaKernel pick_tma_p(int P)
     case 128: return tma_instance<MODE, 128>();
     case 144: return tma_instance<MODE, 144>(); // two racks
     case 256: return tma_instance<MODE, 256>();
-    default: // measured: 256 consumers, as P = 8 takes, cost P = 5-7 20 %
-        if (P <= 4) return tma_generic<MODE, tma_threads(4)>();
-        return tma_generic<MODE, tma_threads(64)>();
+    default: // P > 8
+        return tma_generic<MODE>(P);
     }
 }
 
