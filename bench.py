@@ -221,9 +221,11 @@ def kernel_source_hash() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, kernel: str = "zero_fused_step_tma_kernel") -> float | None:
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    if it was taken on the current kernel source and of the kernel the step
+def profiled_traffic(workload: str, kernel: str = "zero_fused_step_tma_kernel", mode: int | None = None
+                     ) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary of this workload
+    (the Adam reading's own figure where the summary has one per mode), if
+    it was taken on the current kernel source and of the kernel the step
     launches now."""
     path = os.path.join(PROFILE_DIR, f"zero_fused_step_{workload}.txt")
     try:
@@ -237,6 +239,8 @@ def profiled_traffic(workload: str, kernel: str = "zero_fused_step_tma_kernel") 
             return None
         if not kv.get("kernel", "").startswith(kernel.split(" ")[0]):
             return None
+        if mode is not None and f"traffic_bytes_per_launch_mode{mode}" in kv:
+            return float(kv[f"traffic_bytes_per_launch_mode{mode}"])
         return float(kv["traffic_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
@@ -516,7 +520,7 @@ def roofline_entry(wl, mode, plan, alg_bytes, mean_launch_ms):
     peak, peak_kind = measured_peaks()
     achieved = alg_bytes / (mean_launch_ms / 1e3) / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": profiled_traffic(wl.name, kernel_label(plan)),
+            "frac": achieved / peak, "traffic": profiled_traffic(wl.name, kernel_label(plan), mode),
             "kernel": kernel_label(plan), "ctas": plan["ctas"],
             "peak_kind": f"{peak_kind} HBM copy bandwidth",
             "algorithmic_bytes_per_launch": alg_bytes, "mean_launch_ms": mean_launch_ms}
