@@ -29,9 +29,13 @@ def _dev(codes):
     return torch.from_numpy(np.ascontiguousarray(codes).view(np.int16)).cuda().view(torch.float16)
 
 
-def test_bounded_wait_runs_out_and_the_context_survives(z):
+# P = 8: a compile-time instance, copies issued by one thread; 13 and 33: the
+# run-time-P instance (peeled first / middle / last chunks), copies issued by
+# the lanes of warp 0
+@pytest.mark.parametrize("P", [8, 13, 33])
+def test_bounded_wait_runs_out_and_the_context_survives(z, P):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    P, N = 8, sms * 2048 * 4 + 3
+    N = sms * 2048 * 4 + 3
     stride = synth.round_up(N, 8)
     codes = synth.np_grads(P, N, stride, 1e-3, 12)
     g = _dev(codes)
