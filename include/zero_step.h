@@ -365,11 +365,13 @@ int zero_cpu_adam(const void* grad_fp16, float* master, float* m, float* v, void
  * memory that the caller keeps alive, and leaves alone, until the stream has
  * passed this step.  The call returns at once.  Numerically the step differs
  * from zero_adam_step only in that the gradient mean is rounded to fp16 on
- * its way to the host.  Errors: ZERO_EINVAL (also for a current device
- * numbered 64 or above, which has no slot for the internal streams),
- * ZERO_EALIGN, ZERO_ENOMEM (host bookkeeping), ZERO_ECUDA (pieces enqueued
- * before the failure stay enqueued, and cuda_stream still waits for them
- * when that is possible). */
+ * its way to the host.  Sizes, hyper-parameters, alignment and the
+ * gradients' overlap with grad16_host are checked before anything is
+ * enqueued.  Errors: ZERO_EINVAL (also for a current device numbered 64 or
+ * above, which has no slot for the internal streams), ZERO_EALIGN,
+ * ZERO_EOVERLAP, ZERO_ENOMEM (host bookkeeping), ZERO_ECUDA (pieces
+ * enqueued before the failure stay enqueued, and cuda_stream still waits for
+ * them when that is possible). */
 int zero_offload_step(const void* grads_fp16, int64_t rank_stride, float* master_host, float* m_host,
                       float* v_host, void* grad16_host, void* params16_host, void* params_fp16,
                       int64_t N, int32_t P, int32_t stage, int64_t t, float lr, float beta1,

@@ -229,3 +229,19 @@ def test_mlp4_step_rejects_before_enqueueing(zlib, kw, code):
 @pytest.mark.parametrize("kw,code", MLP_BAD_BOTH)
 def test_mlp4_noalloc_step_rejects_before_enqueueing(zlib, kw, code):
     assert _mlp_noalloc(zlib, **kw) == code
+
+
+@no_gpu
+@pytest.mark.parametrize("kw,code", [
+    (dict(mode=3), -1), (dict(cpu_threads=-1), -1), (dict(rank_stride=999), -1), (dict(g16=None), -1),
+    (dict(master=W + 2), -2), (dict(g16=7 * A + 1), -2), (dict(grads=G + 1), -2), (dict(params=PP + 1), -2),
+    (dict(g16=G + 2 * 2000), -3),
+])
+def test_offload_step_rejects_before_enqueueing(zlib, kw, code):
+    """The offload step checks every buffer before its first CUDA call."""
+    a = dict(grads=G, rank_stride=1000, master=W, m=MM, v=V, g16=7 * A, p16=8 * A, params=PP, N=1000,
+             P=4, mode=0, cpu_threads=0)
+    a.update(kw)
+    assert zlib.lib().zero_offload_step(a["grads"], a["rank_stride"], a["master"], a["m"], a["v"], a["g16"],
+                                        a["p16"], a["params"], a["N"], a["P"], 2, 1, 1e-3, 0.9, 0.999, 1e-8,
+                                        a["mode"], a["cpu_threads"], 0) == code

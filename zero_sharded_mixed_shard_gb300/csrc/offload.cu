@@ -118,10 +118,20 @@ extern "C" int zero_offload_step(const void* grads_fp16, int64_t rank_stride, fl
     if (mode > ZERO_MODE_FOLDED_STORAGE) return ZERO_EINVAL; // the host update is Adam
     if (!grads_fp16 || !master_host || !m_host || !v_host || !grad16_host || !params16_host || !params_fp16)
         return ZERO_EINVAL;
+    // every check the pieces' calls below would make, before anything is
+    // enqueued: a refused call writes nothing
     if (reinterpret_cast<uintptr_t>(master_host) % 4 || reinterpret_cast<uintptr_t>(m_host) % 4 ||
         reinterpret_cast<uintptr_t>(v_host) % 4 || reinterpret_cast<uintptr_t>(params16_host) % 2 ||
-        reinterpret_cast<uintptr_t>(params_fp16) % 2)
+        reinterpret_cast<uintptr_t>(params_fp16) % 2 || reinterpret_cast<uintptr_t>(grads_fp16) % 2 ||
+        reinterpret_cast<uintptr_t>(grad16_host) % 2)
         return ZERO_EALIGN;
+    {
+        const uintptr_t gg = reinterpret_cast<uintptr_t>(grads_fp16);
+        const uintptr_t g_span = (static_cast<uintptr_t>(P - 1) * static_cast<uintptr_t>(rank_stride) +
+                                  static_cast<uintptr_t>(N)) * 2;
+        const uintptr_t h = reinterpret_cast<uintptr_t>(grad16_host), hb = static_cast<uintptr_t>(N) * 2;
+        if (gg < h + hb && h < gg + g_span) return ZERO_EOVERLAP;
+    }
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     OffloadStreams side;
     rc = offload_streams(&side);
