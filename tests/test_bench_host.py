@@ -49,6 +49,22 @@ def test_profile_traffic_requires_matching_source_and_kernel(tmp_path, monkeypat
     f.write_text(head + "source_sha256: 0000\ntraffic_bytes_per_launch: 123\n")
     assert bench.profiled_traffic("gpt2s") is None
     assert bench.profiled_traffic("shard7p5b") is None
+    # a summary with one figure per Adam reading answers each mode with its own
+    g = tmp_path / "zero_fused_step_folded.txt"
+    g.write_text("kernel: zero_fused_step_tma_kernel<1,32,512,2,0>\n"
+                 f"source_sha256: {bench.kernel_source_hash()}\ntraffic_bytes_per_launch: 10\n"
+                 "traffic_bytes_per_launch_mode1: 10\ntraffic_bytes_per_launch_mode2: 20\n")
+    assert bench.profiled_traffic("folded", mode=1) == 10.0
+    assert bench.profiled_traffic("folded", mode=2) == 20.0
+    assert bench.profiled_traffic("folded", mode=0) == 10.0   # no figure of its own: the summary's
+
+
+def test_committed_profiles_match_the_current_kernel_source():
+    """Every committed step summary was taken on the kernel source as it is
+    now (else the bench's traffic would read null)."""
+    for name in ("tiny", "gpt2s", "tf1p3b", "shard7p5b", "folded"):
+        kernel = "zero_fused_step_kernel" if name == "tiny" else "zero_fused_step_tma_kernel"
+        assert bench.profiled_traffic(name, kernel) is not None, name
 
 
 def _free_port():
