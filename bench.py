@@ -128,6 +128,15 @@ class Dist:
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
+    def all_true(self, ok: bool, device=None) -> bool:
+        """True on every rank iff ``ok`` is true on every rank."""
+        if not self.pg:
+            return ok
+        import torch
+        t = torch.tensor([1 if ok else 0], dtype=torch.int32, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MIN)
+        return bool(t.item())
+
     def close(self):
         if self.pg:
             self.pg.destroy_process_group()
@@ -646,11 +655,18 @@ def run_e2e(head, device, dist):
     link, ~200 GB/s)."""
     import torch
     g, params, stream = head.g, head.params, head.stream
+    host_g = host_p = None
+    why = ""
     try:
         host_g = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
         host_p = torch.empty(params.shape, dtype=params.dtype, pin_memory=True)
     except RuntimeError as exc:   # the host could not page-lock that much memory
-        return {"value": None, "unit": "params/s", "unavailable": f"pinned host buffers: {exc}"[:200]}
+        why = f"pinned host buffers: {exc}"[:200]
+    # every rank runs the leg or none does (its barriers must pair up)
+    if not dist.all_true(host_p is not None, device):
+        del host_g, host_p
+        return {"value": None, "unit": "params/s",
+                "unavailable": why or "another rank could not page-lock its host buffers"}
     host_g.copy_(g)
     h2d = host_g.numel() * host_g.element_size()
     K_e2e = max(3, min(100, int(5.0 / (h2d / 200e9 + 1e-4))))

@@ -81,7 +81,9 @@ def _rank_main(rank, world, port, out):
     d.barrier()
     got = d.max(10.0 + rank)
     d.barrier()
-    out.put((rank, d.world, got))
+    both = d.all_true(True)
+    one = d.all_true(rank == 0)     # false on one rank: false on both
+    out.put((rank, d.world, got, both, one))
     d.close()
 
 
@@ -97,7 +99,7 @@ def test_two_gloo_ranks_take_the_slowest_time():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    assert res == [(0, 2, 11.0), (1, 2, 11.0)]
+    assert res == [(0, 2, 11.0, True, False), (1, 2, 11.0, True, False)]
 
 
 def test_reference_arm_other_ranks_do_no_work(monkeypatch):
