@@ -525,6 +525,32 @@ def one_element_step_ms(z, wl, mode, K, dist, device, stream) -> float:
     return ms
 
 
+def ring_step_ms(z, wl, mode, K, dist, device, stream) -> tuple[float, int]:
+    """Steps of R independent copies of a small workload, round-robin and
+    back to back (one event pair around all K steps, no flush): R is chosen
+    so the copies together are 4x the L2, so every step's inputs have left
+    L2 by the time its copy comes round again.  Returns (ms per step, R)."""
+    import torch
+    from zero_sharded_mixed_shard_gb300 import synth
+    R = max(2, -(-4 * L2_BYTES // (wl.elems * synth.bytes_per_elem(wl.P, mode))))
+    legs = [Timed(z, wl, mode, dist, device, stream) for _ in range(R)]
+    for leg in legs:
+        leg.flush = leg.flush_read = None
+        leg.step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        legs[i % R].step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(e0.elapsed_time(e1) / K, device)
+    for leg in legs:
+        leg.free()
+    return ms, R
+
+
 def roofline_entry(wl, mode, plan, alg_bytes, mean_launch_ms):
     peak, peak_kind = measured_peaks()
     achieved = alg_bytes / (mean_launch_ms / 1e3) / 1e9
@@ -596,9 +622,15 @@ def run_ours(args, wl, mode, dist):
             extra = {}
             if leg.flush is not None:   # a small workload: how much of its time is the launch
                 floor = dist.max(one_element_step_ms(z, cwl, cmode, ck, dist, device, stream), device)
+                ring_ms, ring_r = ring_step_ms(z, cwl, cmode, ck, dist, device, stream)
                 extra = {"one_element_step_ms": floor,
                          "gbs_above_one_element_step": leg.alg_bytes / ((l_ms - floor) / 1e3) / 1e9
-                         if l_ms > floor else None}
+                         if l_ms > floor else None,
+                         "back_to_back": {"ms_per_step": ring_ms, "copies": ring_r,
+                                          "gbs": leg.alg_bytes / (ring_ms / 1e3) / 1e9,
+                                          "how": f"{ck} steps round-robin over {ring_r} independent copies "
+                                                 "of the workload (4x the L2 together), one event pair "
+                                                 "around them all, no flush"}}
             per_config[f"{name}/mode{cmode}"] = {
                 "workload": workload_config(cwl, cmode, None if leg.flush is None else leg.flush.numel())["workload"],
                 "value": cwl.elems * ck * dist.world / (r_ms / 1e3), "unit": "params/s", "steps": ck,

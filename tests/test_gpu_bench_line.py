@@ -53,6 +53,9 @@ def test_default_bench_line_has_the_contract_keys():
         assert e["value"] > 0 and e["steps"] >= 20 and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9, name
         assert r["traffic"] is not None, f"{name}: profile summary missing or stale"
     assert pc["tiny/mode0"]["roofline"]["kernel"].startswith("zero_fused_step_kernel")
+    tiny = pc["tiny/mode0"]
+    assert 0 < tiny["one_element_step_ms"] < tiny["roofline"]["mean_launch_ms"]
+    assert tiny["back_to_back"]["ms_per_step"] > 0 and tiny["back_to_back"]["copies"] >= 2
     for name in ("gpt2s/mode0", "shard7p5b/mode0", "folded/mode1", "folded/mode2"):
         assert pc[name]["roofline"]["kernel"] == "zero_fused_step_tma_kernel", name
     assert pc["clocks"]["samples"] >= 1
