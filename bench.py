@@ -72,6 +72,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     ap.add_argument("--no-per-config", action="store_true",
                     help="time the chosen workload only (no per_config block)")
+    ap.add_argument("--unpadded-stride", action="store_true",
+                    help="rank stride = the elements of a rank's slice, not rounded up to a multiple of 8 "
+                         "(rows off the 16-byte phase: the phased pipeline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=24.0,
                     help="wall time budget of the CPU-oracle leg (all of its runs together)")
@@ -439,13 +442,13 @@ class Timed:
     timing of K steps after W warm-up steps (CUDA events on the launching
     stream, one pair per step)."""
 
-    def __init__(self, z, wl, mode, dist, device, stream):
+    def __init__(self, z, wl, mode, dist, device, stream, padded=True):
         import torch
 
         from zero_sharded_mixed_shard_gb300 import synth
         self.z, self.wl, self.mode, self.dist, self.stream = z, wl, mode, dist, stream
         E, P = wl.elems, wl.P
-        self.stride = wl.rank_stride(True)
+        self.stride = wl.rank_stride(padded)
         self.g = synth.torch_grads(P, E, self.stride, wl.grad_sigma, wl.seed + 17 * dist.rank, device,
                                    wl.heavy_tail_frac, wl.zero_frac, step=1)
         self.master, self.m, self.v, self.params = synth.torch_state(E, wl.seed + 17 * dist.rank, device,
@@ -575,7 +578,7 @@ def run_ours(args, wl, mode, dist):
     z.lib()
     stream = torch.cuda.current_stream(device)
 
-    head = Timed(z, wl, mode, dist, device, stream)
+    head = Timed(z, wl, mode, dist, device, stream, padded=not args.unpadded_stride)
     head.warm(args.warmup)
     K = args.steps
     sampler = ClockSampler(dist.local_rank)
@@ -604,7 +607,7 @@ def run_ours(args, wl, mode, dist):
     # every other workload, in the same run and under the same clock sampler
     per_config = None
     p0 = p1 = None
-    if not args.no_per_config and args.ranks is None and args.elements is None:
+    if not args.no_per_config and args.ranks is None and args.elements is None and not args.unpadded_stride:
         per_config = {}
         p0 = time.time()
         for name, cmode in ALL_CONFIGS:
@@ -659,7 +662,8 @@ def run_ours(args, wl, mode, dist):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "io_dtypes": "fp16 gradients and parameters, fp32 master/m/v",
             "data": "synthetic (seeded device RNG)",
-            "config": workload_config(wl, mode, l2_flush_bytes=flush_bytes),
+            "config": dict(workload_config(wl, mode, l2_flush_bytes=flush_bytes),
+                           **({"rank_stride": wl.rank_stride(False)} if args.unpadded_stride else {})),
             "achieved_hbm_gbs": alg_bytes * K * dist.world / (region_ms / 1e3) / 1e9,
             "pct_of_nominal_8tbs": 100 * alg_bytes * K / (region_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
             "roofline": roofline_entry(wl, mode, plan, alg_bytes, mean_launch_ms),
