@@ -49,6 +49,9 @@ DEFAULT_STEPS = {"tiny": 20000, "gpt2s": 2500, "tf1p3b": 200, "shard7p5b": 800, 
 # every workload with each Adam reading it runs; the headline is one of them,
 # the rest go to the line's per_config block
 ALL_CONFIGS = (("tiny", 0), ("gpt2s", 0), ("tf1p3b", 0), ("shard7p5b", 0), ("folded", 1), ("folded", 2))
+# also timed in per_config: the 7.5B shard in its natural packed layout, rank
+# stride M = 117,187,500 elements (4 mod 8: the vector kernel at width 4)
+UNPADDED_CONFIGS = (("shard7p5b", 0),)
 # timed steps of a per_config leg: at least this many (about 0.2 s of GPU time)
 PER_CONFIG_MIN_STEPS = {"tiny": 2000, "gpt2s": 250, "tf1p3b": 20, "shard7p5b": 80, "folded": 60}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
@@ -610,11 +613,13 @@ def run_ours(args, wl, mode, dist):
     if not args.no_per_config and args.ranks is None and args.elements is None and not args.unpadded_stride:
         per_config = {}
         p0 = time.time()
-        for name, cmode in ALL_CONFIGS:
-            if (name, cmode) == (wl.name, mode):
-                continue
+        legs = [(n, cm, True) for n, cm in ALL_CONFIGS if (n, cm) != (wl.name, mode)]
+        legs += [(n, cm, False) for n, cm in UNPADDED_CONFIGS]
+        for name, cmode, padded in legs:
             cwl = synth.WORKLOADS[name]
-            leg = Timed(z, cwl, cmode, dist, device, stream)
+            if not padded:
+                cwl = dataclasses.replace(cwl, name=f"{name}-unpadded")
+            leg = Timed(z, cwl, cmode, dist, device, stream, padded=padded)
             leg.warm(args.warmup)
             ck = max(K, PER_CONFIG_MIN_STEPS[name])
             dist.barrier()
@@ -634,8 +639,9 @@ def run_ours(args, wl, mode, dist):
                                           "how": f"{ck} steps round-robin over {ring_r} independent copies "
                                                  "of the workload (4x the L2 together), one event pair "
                                                  "around them all, no flush"}}
-            per_config[f"{name}/mode{cmode}"] = {
-                "workload": workload_config(cwl, cmode, None if leg.flush is None else leg.flush.numel())["workload"],
+            per_config[f"{name}/mode{cmode}" + ("" if padded else "/unpadded")] = {
+                "workload": workload_config(cwl, cmode, None if leg.flush is None else leg.flush.numel())["workload"]
+                            + ("" if padded else f", rank stride {leg.stride:,}"),
                 "value": cwl.elems * ck * dist.world / (r_ms / 1e3), "unit": "params/s", "steps": ck,
                 "ms_per_step": r_ms / ck,
                 "roofline": roofline_entry(cwl, cmode, leg.plan, leg.alg_bytes, l_ms),

@@ -62,8 +62,8 @@ def test_profile_traffic_requires_matching_source_and_kernel(tmp_path, monkeypat
 def test_committed_profiles_match_the_current_kernel_source():
     """Every committed step summary was taken on the kernel source as it is
     now (else the bench's traffic would read null)."""
-    for name in ("tiny", "gpt2s", "tf1p3b", "shard7p5b", "folded"):
-        kernel = "zero_fused_step_kernel" if name == "tiny" else "zero_fused_step_tma_kernel"
+    for name in ("tiny", "gpt2s", "tf1p3b", "shard7p5b", "folded", "shard7p5b-unpadded"):
+        kernel = "zero_fused_step_kernel" if name in ("tiny", "shard7p5b-unpadded") else "zero_fused_step_tma_kernel"
         assert bench.profiled_traffic(name, kernel) is not None, name
 
 

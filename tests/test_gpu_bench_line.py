@@ -44,8 +44,8 @@ def test_default_bench_line_has_the_contract_keys():
     ck = d["clocks"]
     assert "sm_mhz" in ck and "sm_max_mhz" in ck and isinstance(ck["reasons"], list)
     pc = d["per_config"]
-    assert set(pc) == {"tiny/mode0", "gpt2s/mode0", "shard7p5b/mode0", "folded/mode1", "folded/mode2",
-                       "clocks"}
+    assert set(pc) == {"tiny/mode0", "gpt2s/mode0", "shard7p5b/mode0", "shard7p5b/mode0/unpadded",
+                       "folded/mode1", "folded/mode2", "clocks"}
     for name, e in pc.items():
         if name == "clocks":
             continue
@@ -58,4 +58,5 @@ def test_default_bench_line_has_the_contract_keys():
     assert tiny["back_to_back"]["ms_per_step"] > 0 and tiny["back_to_back"]["copies"] >= 2
     for name in ("gpt2s/mode0", "shard7p5b/mode0", "folded/mode1", "folded/mode2"):
         assert pc[name]["roofline"]["kernel"] == "zero_fused_step_tma_kernel", name
+    assert pc["shard7p5b/mode0/unpadded"]["roofline"]["kernel"] == "zero_fused_step_kernel (vector width 4)"
     assert pc["clocks"]["samples"] >= 1
