@@ -322,11 +322,28 @@ __device__ __forceinline__ void step_elems(const StepArgs& a, long long i)
         for (int u = 0; u < kRankBatch; ++u) accumulate<V>(acc, buf[u]);
         gp += (long long)kRankBatch * a.stride;
     }
-    constexpr int kInner = PT > 0 ? kRankBatch : 1;
+    if constexpr (PT > 0 || V == 8 || V == 1) {
+        constexpr int kInner = PT > 0 ? kRankBatch : 1;
 #pragma unroll kInner
-    for (; r < P; ++r) {
-        accumulate<V>(acc, load_halves<V>(gp));
-        gp += a.stride;
+        for (; r < P; ++r) {
+            accumulate<V>(acc, load_halves<V>(gp));
+            gp += a.stride;
+        }
+    } else {
+        // the last P mod 8 ranks, a count known only at run time: their loads
+        // issued together under predicates, then summed in rank order
+        // (measured, rows off the 16-byte phase, width 4: P = 3 0.78 -> 0.98,
+        // 5 0.73 -> 0.94, 12 0.84 -> 0.97 of the copy roofline; width 2
+        // alike.  At width 8 the buffer spills, at width 1 it costs CTAs per
+        // SM: both keep the one-rank loop)
+        const int rem = P - r;
+        HalfRaw<V> buf[kRankBatch];
+#pragma unroll
+        for (int u = 0; u < kRankBatch; ++u)
+            if (u < rem) buf[u] = load_halves<V>(gp + (long long)u * a.stride);
+#pragma unroll
+        for (int u = 0; u < kRankBatch; ++u)
+            if (u < rem) accumulate<V>(acc, buf[u]);
     }
 
 #pragma unroll
@@ -776,9 +793,13 @@ KernelFn pick_p(int P)
         case 64: return zero_fused_step_kernel<MODE, 8, 64>;
         default: return zero_fused_step_kernel<MODE, 8, 0>;
         }
-    } else {
+    } else if constexpr (V == 4) {
         (void)P;
         return zero_fused_step_kernel<MODE, V, 0>;
+    } else {
+        // P = 4 compiled in at widths 2 and 1 (rows off the 16-byte phase):
+        // 0.67 -> 1.00 and 0.47 -> 0.84 of the copy roofline
+        return P == 4 ? zero_fused_step_kernel<MODE, V, 4> : zero_fused_step_kernel<MODE, V, 0>;
     }
 }
 
