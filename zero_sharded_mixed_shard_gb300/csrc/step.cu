@@ -673,12 +673,40 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
     // Wait for unit uu's stage (every thread), then refill the stage of
     // unit uu-1, which every thread has finished once the barrier passes.
     // False if the wait gave up (one decision for the whole CTA).
-    auto wait_unit = [&](long long uu) -> bool {
+    // When a stage is refilled.  Late (one or two chunks per tile): once
+    // every thread has passed the wait for unit uu, the stage of unit uu-1
+    // (whose last reader was the Adam of that unit).  Early (three chunks or
+    // more): once every thread has read unit uu's rows into registers, that
+    // unit's own stage, so four units are in flight during the arithmetic
+    // instead of three.  Measured, fraction of the copy roofline: early P =
+    // 32 1.018 -> 1.066, 64 0.997 -> 1.037, 24 1.004 -> 1.019; P = 16 even;
+    // and worse with fewer chunks (P = 8 0.977 -> 0.888, 12 0.913 -> 0.885).
+    // Either way one barrier per unit, which also makes a wait that gave up
+    // one decision for the whole CTA.
+    // (a compile-time choice inside the loops below: EARLY is a template
+    // argument of the consumer)
+    const bool early = PT > 0 ? PT > 2 * kChunkRanks : nch > 2;
+    auto wait_full = [&](long long uu) -> bool {
         const int s = static_cast<int>(uu % kStages);
-        const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>((uu / kStages) & 1));
-        if (__syncthreads_or(!ok)) return false;
-        if (tid < 32 && uu >= 1 && uu - 1 + kStages < units) issue(uu - 1 + kStages);
-        return true;
+        return mbar_wait_bounded(&full[s], static_cast<uint32_t>((uu / kStages) & 1));
+    };
+    auto before_read = [&](auto early_tag, long long uu, bool ok) -> bool { // late refill
+        if constexpr (decltype(early_tag)::value) {
+            return true;
+        } else {
+            if (__syncthreads_or(!ok)) return false;
+            if (tid < 32 && uu >= 1 && uu - 1 + kStages < units) issue(uu - 1 + kStages);
+            return true;
+        }
+    };
+    auto after_read = [&](auto early_tag, long long uu, bool ok) -> bool { // early refill
+        if constexpr (!decltype(early_tag)::value) {
+            return true;
+        } else {
+            if (__syncthreads_or(!ok)) return false;
+            if (tid < 32 && uu + kStages < units) issue(uu + kStages);
+            return true;
+        }
     };
     auto stage_of = [&](long long uu) { return smem + static_cast<size_t>(uu % kStages) * kStageBytes; };
     auto load_state = [&](const unsigned char* st) {
@@ -689,77 +717,118 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
         if constexpr (uses_v(MODE)) smem_floats<E>(st + kGradBytes + 2 * kTile * 4 + e0 * 4, v);
     };
 
-    if constexpr (PT > 0) {
-        for (; u < units; ++u) {
-            if (!wait_unit(u)) {
-                failed = true;
-                break;
-            }
-            const int c = static_cast<int>(u % nch);
-            const long long i0 = tile_of(u) * kTile;
-            const long long len = nbulk - i0 < kTile ? nbulk - i0 : kTile;
-            const unsigned char* st = stage_of(u);
-            if (e0 < len) {
-                if (c == 0) load_state(st);
-                // ranks c*8 .. c*8+rc-1 of this tile, in rank order
-                const int rc = P - c * kChunkRanks < kChunkRanks ? P - c * kChunkRanks : kChunkRanks;
-#pragma unroll
-                for (int q = 0; q < kChunkRanks; ++q)
-                    if (q < rc) accumulate<E>(acc, smem_halves<E>(st + static_cast<size_t>(q) * kTile * 2 + e0 * 2));
-                if (c == nch - 1) finish_tile<MODE, PT, E, G>(a, acc, w, m, v, i0 + e0, w0, m0, v0, p0);
-            }
-        }
-    } else {
-        // Run-time P: each tile's units walked as its first chunk (with the
-        // state rows), the full middle chunks and the last chunk of RL
-        // ranks, so every chunk's rank count is known where it is summed.
-        for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-            const long long i0 = tile * kTile;
-            const long long len = nbulk - i0 < kTile ? nbulk - i0 : kTile;
-            const bool mine = e0 < len;
-            if (!wait_unit(u)) {
-                failed = true;
-                break;
-            }
-            const unsigned char* st = stage_of(u);
-            if (nch == 1) { // P = RL: one unit per tile
-                if (mine) {
-                    load_state(st);
-                    accumulate_rows<E, RL>(acc, st + static_cast<size_t>(e0) * 2);
-                    finish_tile<MODE, PT, E, G>(a, acc, w, m, v, i0 + e0, w0, m0, v0, p0);
-                }
-                ++u;
-                continue;
-            }
-            if (mine) {
-                load_state(st);
-                accumulate_rows<E, kChunkRanks>(acc, st + static_cast<size_t>(e0) * 2);
-            }
-            ++u;
-            for (int c = 1; c < nch - 1; ++c, ++u) {
-                if (!wait_unit(u)) {
+    auto consume = [&](auto early_tag) {
+        if constexpr (PT > 0) {
+            for (; u < units; ++u) {
+                const bool ok = wait_full(u);
+                if (!before_read(early_tag, u, ok)) {
                     failed = true;
                     break;
                 }
-                if (mine) accumulate_rows<E, kChunkRanks>(acc, stage_of(u) + static_cast<size_t>(e0) * 2);
+                const int c = static_cast<int>(u % nch);
+                const long long i0 = tile_of(u) * kTile;
+                const long long len = nbulk - i0 < kTile ? nbulk - i0 : kTile;
+                const unsigned char* st = stage_of(u);
+                constexpr bool kEarly = decltype(early_tag)::value;
+                if (e0 < len) {
+                    if (c == 0) load_state(st);
+                    // ranks c*8 .. c*8+rc-1 of this tile, in rank order
+                    const int rc = P - c * kChunkRanks < kChunkRanks ? P - c * kChunkRanks : kChunkRanks;
+#pragma unroll
+                    for (int q = 0; q < kChunkRanks; ++q)
+                        if (q < rc) accumulate<E>(acc, smem_halves<E>(st + static_cast<size_t>(q) * kTile * 2 + e0 * 2));
+                    if constexpr (!kEarly)
+                        if (c == nch - 1) finish_tile<MODE, PT, E, G>(a, acc, w, m, v, i0 + e0, w0, m0, v0, p0);
+                }
+                if constexpr (kEarly) {
+                    if (!after_read(early_tag, u, ok)) {
+                        failed = true;
+                        break;
+                    }
+                    if (e0 < len && c == nch - 1) finish_tile<MODE, PT, E, G>(a, acc, w, m, v, i0 + e0, w0, m0, v0, p0);
+                }
             }
-            if (failed) break;
-            if (!wait_unit(u)) {
-                failed = true;
-                break;
+        } else {
+            // Run-time P: each tile's units walked as its first chunk (with the
+            // state rows), the full middle chunks and the last chunk of RL
+            // ranks, so every chunk's rank count is known where it is summed.
+            for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+                const long long i0 = tile * kTile;
+                const long long len = nbulk - i0 < kTile ? nbulk - i0 : kTile;
+                const bool mine = e0 < len;
+                bool ok = wait_full(u);
+                if (!before_read(early_tag, u, ok)) {
+                    failed = true;
+                    break;
+                }
+                const unsigned char* st = stage_of(u);
+                if (nch == 1) { // P = RL: one unit per tile (the late refill)
+                    if (mine) {
+                        load_state(st);
+                        accumulate_rows<E, RL>(acc, st + static_cast<size_t>(e0) * 2);
+                        finish_tile<MODE, PT, E, G>(a, acc, w, m, v, i0 + e0, w0, m0, v0, p0);
+                    }
+                    ++u;
+                    continue;
+                }
+                if (mine) {
+                    load_state(st);
+                    accumulate_rows<E, kChunkRanks>(acc, st + static_cast<size_t>(e0) * 2);
+                }
+                if (!after_read(early_tag, u, ok)) {
+                    failed = true;
+                    break;
+                }
+                ++u;
+                for (int c = 1; c < nch - 1; ++c, ++u) {
+                    ok = wait_full(u);
+                    if (!before_read(early_tag, u, ok)) {
+                        failed = true;
+                        break;
+                    }
+                    if (mine) accumulate_rows<E, kChunkRanks>(acc, stage_of(u) + static_cast<size_t>(e0) * 2);
+                    if (!after_read(early_tag, u, ok)) {
+                        failed = true;
+                        break;
+                    }
+                }
+                if (failed) break;
+                ok = wait_full(u);
+                if (!before_read(early_tag, u, ok)) {
+                    failed = true;
+                    break;
+                }
+                if constexpr (decltype(early_tag)::value) {
+                    if (mine) accumulate_rows<E, RL>(acc, stage_of(u) + static_cast<size_t>(e0) * 2);
+                    if (!after_read(early_tag, u, ok)) {
+                        failed = true;
+                        break;
+                    }
+                    if (mine) finish_tile<MODE, PT, E, G>(a, acc, w, m, v, i0 + e0, w0, m0, v0, p0);
+                } else if (mine) {
+                    accumulate_rows<E, RL>(acc, stage_of(u) + static_cast<size_t>(e0) * 2);
+                    finish_tile<MODE, PT, E, G>(a, acc, w, m, v, i0 + e0, w0, m0, v0, p0);
+                }
+                ++u;
             }
-            if (mine) {
-                accumulate_rows<E, RL>(acc, stage_of(u) + static_cast<size_t>(e0) * 2);
-                finish_tile<MODE, PT, E, G>(a, acc, w, m, v, i0 + e0, w0, m0, v0, p0);
-            }
-            ++u;
         }
+    };
+    if constexpr (PT > 0) {
+        consume(std::integral_constant<bool, (PT > 2 * kChunkRanks)>{});
+    } else {
+        if (early)
+            consume(std::true_type{});
+        else
+            consume(std::false_type{});
     }
 
     if (failed && tid == 0) {
         // let the copies already issued land before the CTA's shared memory goes away
-        const long long issued_end = (u >= 1 ? u - 1 : 0) + kStages < units ? (u >= 1 ? u - 1 : 0) + kStages
-                                                                              : units;
+        // units issued so far: up to u - 2 + kStages with the late refill (unit
+        // j's wait refilled the stage of j - 1), up to u - 1 + kStages with the
+        // early one (unit j's reads refilled its own stage)
+        const long long next = (early ? u : (u >= 1 ? u - 1 : 0)) + kStages;
+        const long long issued_end = next < units ? next : units;
         for (long long k = u; k < issued_end; ++k)
             (void)mbar_wait_bounded(&full[k % kStages], static_cast<uint32_t>((k / kStages) & 1));
         atomicAdd(&g_wait_timeouts, 1u);
