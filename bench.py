@@ -231,8 +231,15 @@ def measured_peaks() -> tuple[float, str]:
 
 
 def kernel_source_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the kernel source's code: comments and blank space taken out,
+    so a summary stays valid across edits that change no code."""
+    import re
+    with open(KERNEL_SRC, encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)      # block comments
+    text = re.sub(r"//[^\n]*", " ", text)                    # line comments
+    text = " ".join(text.split())
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
 
 
 def profiled_traffic(workload: str, kernel: str = "zero_fused_step_tma_kernel", mode: int | None = None

@@ -176,3 +176,16 @@ def test_oracle_inputs_repeat_a_draw_to_fill_a_sample():
     c = codes.reshape(wl.P, 10_000)
     assert np.array_equal(c[:, 4096:8192], c[:, :4096]) and np.array_equal(w[4096:8192], w[:4096])
     assert not m.any() and not v.any() and codes.size == wl.P * 10_000
+
+
+def test_kernel_source_hash_ignores_comments_only(tmp_path, monkeypatch):
+    """A profile summary is keyed to the kernel's code: comment and spacing
+    edits keep the key, a code edit changes it."""
+    f = tmp_path / "k.cu"
+    monkeypatch.setattr(bench, "KERNEL_SRC", str(f))
+    f.write_text("int f(int x) { return x + 1; } // one\n")
+    h0 = bench.kernel_source_hash()
+    f.write_text("/* a new\n block */ int f(int x)  {\n  return x + 1; // two\n}\n")
+    assert bench.kernel_source_hash() == h0
+    f.write_text("int f(int x) { return x + 2; }\n")
+    assert bench.kernel_source_hash() != h0

@@ -670,21 +670,19 @@ __global__ void __launch_bounds__(NT, 1) zero_fused_step_tma_kernel(const StepAr
     long long u = 0;
     bool failed = false;
     const int e0 = tid * E;
-    // Wait for unit uu's stage (every thread), then refill the stage of
-    // unit uu-1, which every thread has finished once the barrier passes.
-    // False if the wait gave up (one decision for the whole CTA).
     // When a stage is refilled.  Late (one or two chunks per tile): once
     // every thread has passed the wait for unit uu, the stage of unit uu-1
     // (whose last reader was the Adam of that unit).  Early (three chunks or
     // more): once every thread has read unit uu's rows into registers, that
     // unit's own stage, so four units are in flight during the arithmetic
     // instead of three.  Measured, fraction of the copy roofline: early P =
-    // 32 1.018 -> 1.066, 64 0.997 -> 1.037, 24 1.004 -> 1.019; P = 16 even;
+    // 32 1.018 -> 1.063, 64 0.997 -> 1.036, 24 1.005 -> 0.988; P = 16 even;
     // and worse with fewer chunks (P = 8 0.977 -> 0.888, 12 0.913 -> 0.885).
     // Either way one barrier per unit, which also makes a wait that gave up
-    // one decision for the whole CTA.
-    // (a compile-time choice inside the loops below: EARLY is a template
-    // argument of the consumer)
+    // one decision for the whole CTA (before_read / after_read return false).
+    // The consumer loop below is instantiated for each choice (early_tag), so
+    // the choice costs nothing inside it; read there as a run-time flag it
+    // cost P = 8 5 %.
     const bool early = PT > 0 ? PT > 2 * kChunkRanks : nch > 2;
     auto wait_full = [&](long long uu) -> bool {
         const int s = static_cast<int>(uu % kStages);
