@@ -18,6 +18,7 @@ import pytest
 
 import oracle
 from _helpers import assert_close, max_ulps
+from _windows import windows
 from zero_sharded_mixed_shard_gb300 import synth
 
 torch = pytest.importorskip("torch")
@@ -31,58 +32,6 @@ def z(zlib, oracle_mod):
         pytest.fail("the GPU tests need a CUDA device")
     yield zlib
     torch.cuda.empty_cache()
-
-
-TILE = 2048          # elements per tile of the bulk-copy pipeline
-
-
-def windows(wl, seed=0, ctas=None, n_random=64, random_len=1 << 20):
-    E = wl.elems
-    r = []
-    if wl.shard is None:
-        for k in range(wl.P):
-            b, e = min(k * wl.M, wl.N), min((k + 1) * wl.M, wl.N)
-            if b < e:
-                r += [(b, min(b + 4096, e)), (max(b, e - 4096), e)]
-    else:
-        r += [(0, min(4096, E)), (max(0, E - 4096), E)]
-    if wl.tensors:
-        pos = 0
-        for n in wl.tensors[:-1]:
-            pos += n
-            r.append((max(0, pos - 256), min(E, pos + 256)))
-    if ctas:
-        # CTA c takes tiles c, c + ctas, ...: its last one is the largest such
-        # index below the tile count (buffers start 16-byte aligned: no head)
-        ntiles = -(-(E // 8 * 8) // TILE)
-        for c in range(min(ctas, ntiles)):
-            last = c + ((ntiles - 1 - c) // ctas) * ctas
-            r.append((last * TILE, min(E, (last + 1) * TILE)))
-    rng = np.random.default_rng(seed)
-    for s in rng.integers(0, max(1, E - random_len), size=n_random):
-        r.append((int(s), int(min(E, s + random_len))))
-    r.sort()
-    merged = []
-    for b, e in r:
-        if merged and b <= merged[-1][1]:
-            merged[-1] = (merged[-1][0], max(merged[-1][1], e))
-        else:
-            merged.append((b, e))
-    return merged
-
-
-@pytest.mark.gpu
-def test_windows_cover_every_cta_last_tile():
-    """Host-side check of the window plan on the 1.3e9 vector at 152 CTAs."""
-    wl = synth.WORKLOADS["tf1p3b"]
-    w = windows(wl, 0, ctas=152)
-    ntiles = -(-wl.N // TILE)
-    for c in range(152):
-        last = c + ((ntiles - 1 - c) // 152) * 152
-        assert last + 152 >= ntiles
-        b = last * TILE
-        assert any(lo <= b and min(wl.N, b + TILE) <= hi for lo, hi in w), c
-    assert sum(e - b for b, e in w) >= 64 * (1 << 20) * 0.9
 
 
 def host_u16(t):
