@@ -451,7 +451,7 @@ class Timed:
     timing of K steps after W warm-up steps (CUDA events on the launching
     stream, one pair per step)."""
 
-    def __init__(self, z, wl, mode, dist, device, stream, padded=True):
+    def __init__(self, z, wl, mode, dist, device, stream, padded=True, flush=True):
         import torch
 
         from zero_sharded_mixed_shard_gb300 import synth
@@ -467,7 +467,7 @@ class Timed:
         self.plan = z.zero_step_plan(self.g, self.stride, self.master, self.m, self.v, self.params, E, P,
                                      wl.stage, mode)
         self.alg_bytes = E * synth.bytes_per_elem(P, mode)
-        fb = l2_flush_for(wl, mode)
+        fb = l2_flush_for(wl, mode) if flush else None
         self.flush = torch.empty(fb, dtype=torch.uint8, device=device) if fb else None
         self.flush_read = torch.ones(fb // 4, dtype=torch.float32, device=device) if fb else None
         self.t = 0
@@ -524,13 +524,8 @@ def one_element_step_ms(z, wl, mode, K, dist, device, stream) -> float:
     P and mode, under the same L2 flush: the fixed cost of a launch through
     the library (enqueue to completion), against which a small workload's
     own time can be read."""
-    import torch
     one = dataclasses.replace(wl, N=1, shard=None, tensors=None, name=wl.name + "-N1")
-    leg = Timed(z, one, mode, dist, device, stream)
-    if leg.flush is None:          # flush as the small workload does
-        fb = 4 * L2_BYTES
-        leg.flush = torch.empty(fb, dtype=torch.uint8, device=device)
-        leg.flush_read = torch.ones(fb // 4, dtype=torch.float32, device=device)
+    leg = Timed(z, one, mode, dist, device, stream)   # flushed like any step below 2x the L2
     leg.warm(3)
     _, ms = leg.run(K)
     leg.free()
@@ -545,9 +540,8 @@ def ring_step_ms(z, wl, mode, K, dist, device, stream) -> tuple[float, int]:
     import torch
     from zero_sharded_mixed_shard_gb300 import synth
     R = max(2, -(-4 * L2_BYTES // (wl.elems * synth.bytes_per_elem(wl.P, mode))))
-    legs = [Timed(z, wl, mode, dist, device, stream) for _ in range(R)]
+    legs = [Timed(z, wl, mode, dist, device, stream, flush=False) for _ in range(R)]
     for leg in legs:
-        leg.flush = leg.flush_read = None
         leg.step()
     torch.cuda.synchronize()
     dist.barrier()
