@@ -21,6 +21,11 @@ def test_defaults():
     assert not a.no_per_config
     with pytest.raises(SystemExit):
         bench.parse_args(["--warmup", "2"])
+    a = bench.parse_args(["--unpadded-stride", "--no-per-config", "--workload", "shard7p5b"])
+    assert a.unpadded_stride and a.no_per_config and a.workload == "shard7p5b"
+    # the unpadded stride of the 7.5B shard is its natural packed length, 4 mod 8
+    from zero_sharded_mixed_shard_gb300 import synth
+    assert synth.WORKLOADS["shard7p5b"].rank_stride(False) % 8 == 4
 
 
 def test_clock_parser_keeps_samples_of_the_timed_region():
